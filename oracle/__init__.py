@@ -1,0 +1,167 @@
+"""qlin oracle: TEST INFRASTRUCTURE ONLY.
+
+A plain CPU restatement (C, fp64 / exact integer arithmetic) of the 8-bit
+quantized linear layer: per-output-channel weight quantizers (INT8 and OCP
+E4M3), the static activation scale from a calibration batch, static activation
+quantization, the exact INT8 accumulator and the fp64 W8A8 / W8A16 references.
+The C source ``qlin_oracle.c`` cites the passages it follows.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  It shares no code with the CUDA library; the product
+path never loads it.  Every function is pinned by a not-gpu test.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qlin_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+INT8 = 0
+E4M3 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2 -fopenmp, no fast-math, no contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_decode.restype = ctypes.c_double
+            L.orc_e4m3_encode.argtypes = [ctypes.c_double]
+            L.orc_e4m3_encode.restype = ctypes.c_uint8
+            L.orc_quantize_weight.argtypes = [I, I64, I64, P, P, P]
+            L.orc_quantize_weight.restype = None
+            L.orc_act_scale.argtypes = [I, I64, I64, P]
+            L.orc_act_scale.restype = ctypes.c_float
+            L.orc_quantize_act.argtypes = [I, I64, I64, P, ctypes.c_float, P]
+            L.orc_quantize_act.restype = None
+            L.orc_i8_gemm.argtypes = [I64, I64, I64, P, P, P]
+            L.orc_i8_gemm.restype = I64
+            L.orc_w8a8.argtypes = [I, I64, I64, I64, P, ctypes.c_float, P, P, P, P, I64, P]
+            L.orc_w8a8.restype = None
+            L.orc_w8a16.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, P]
+            L.orc_w8a16.restype = None
+            L.orc_num_threads.argtypes = []
+            L.orc_num_threads.restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a)
+    assert a.dtype == dtype, (a.dtype, dtype)
+    return a
+
+
+def e4m3_decode(code: int) -> float:
+    return lib().orc_e4m3_decode(int(code) & 0xFF)
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().orc_e4m3_encode(float(v)))
+
+
+def quantize_weight(qtype: int, w: np.ndarray):
+    """w: float32 [N,K] -> (q uint8 [N,K] (int8 bits or E4M3 codes), s float32 [N])."""
+    w = _c(w, np.float32)
+    N, K = w.shape
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((N,), np.float32)
+    lib().orc_quantize_weight(qtype, N, K, _ptr(w), _ptr(q), _ptr(s))
+    return q, s
+
+
+def act_scale(qtype: int, x_cal_bf16: np.ndarray) -> np.float32:
+    """x_cal: uint16 BF16 bits [rows,K] -> fp32 per-tensor input scale."""
+    x = _c(x_cal_bf16, np.uint16)
+    rows, K = x.shape
+    return np.float32(lib().orc_act_scale(qtype, rows, K, _ptr(x)))
+
+
+def quantize_act(qtype: int, x_bf16: np.ndarray, s_x) -> np.ndarray:
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    lib().orc_quantize_act(qtype, M, K, _ptr(x), ctypes.c_float(float(np.float32(s_x))), _ptr(q))
+    return q
+
+
+def i8_gemm(qx: np.ndarray, qw: np.ndarray) -> np.ndarray:
+    """Exact int32 accumulator sum_k qx[m,k]*qw[n,k] (int8 inputs)."""
+    qx = _c(qx.view(np.int8), np.int8)
+    qw = _c(qw.view(np.int8), np.int8)
+    M, K = qx.shape
+    N, K2 = qw.shape
+    assert K == K2
+    acc = np.empty((M, N), np.int32)
+    bad = lib().orc_i8_gemm(M, K, N, _ptr(qx), _ptr(qw), _ptr(acc))
+    if bad:
+        raise OverflowError(f"{bad} accumulator entries exceed int32")
+    return acc
+
+
+def _rows(rows, M):
+    if rows is None:
+        return None, M
+    r = np.ascontiguousarray(np.asarray(rows, np.int64))
+    assert r.ndim == 1 and (r.size == 0 or (r.min() >= 0 and r.max() < M))
+    return r, r.size
+
+
+def w8a8(qtype: int, qx, s_x, qw, s_w, bias=None, rows=None) -> np.ndarray:
+    """fp64 W8A8 reference y[rows or all, N]."""
+    qx = _c(qx, np.uint8)
+    qw = _c(qw, np.uint8)
+    s_w = _c(s_w, np.float32)
+    M, K = qx.shape
+    N = qw.shape[0]
+    b = None if bias is None else _c(bias, np.uint16)
+    r, R = _rows(rows, M)
+    y = np.empty((R, N), np.float64)
+    lib().orc_w8a8(qtype, M, K, N, _ptr(qx), ctypes.c_float(float(np.float32(s_x))), _ptr(qw),
+                   _ptr(s_w), _ptr(b), _ptr(r), R, _ptr(y))
+    return y
+
+
+def w8a16(qtype: int, x_bf16, qw, s_w, bias=None, rows=None) -> np.ndarray:
+    """fp64 W8A16 reference y[rows or all, N]."""
+    x = _c(x_bf16, np.uint16)
+    qw = _c(qw, np.uint8)
+    s_w = _c(s_w, np.float32)
+    M, K = x.shape
+    N = qw.shape[0]
+    b = None if bias is None else _c(bias, np.uint16)
+    r, R = _rows(rows, M)
+    y = np.empty((R, N), np.float64)
+    lib().orc_w8a16(qtype, M, K, N, _ptr(x), _ptr(qw), _ptr(s_w), _ptr(b), _ptr(r), R, _ptr(y))
+    return y
+
+
+def num_threads() -> int:
+    return int(lib().orc_num_threads())

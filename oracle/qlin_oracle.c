@@ -1,0 +1,229 @@
+/*
+ * qlin oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU restatement of what the 8-bit quantized
+ * linear layer computes.  Only the test suite, the smoke check and the timed CPU
+ * baseline of the benchmark may load this file.  It shares no code, header,
+ * table or constant with the CUDA library and includes no CUDA header.
+ *
+ * Sources (page titles as printed):
+ *   [P1] "Nano-vLLM-MoE" README (English), sections "FP8 W8A16 weight-only
+ *        quantization" (Setup: Triton FP8->BF16 dequant GEMM, bf16 x bf16 with
+ *        fp32 accumulation) and "FP8 W8A8 static quantization" (Setup: export
+ *        with offline-calibrated activation scales; _scaled_mm / CUTLASS linear
+ *        backends with a custom epilogue).
+ *   [P2] "Nano-vLLM-MOE" README (Chinese), section "INT8 量化支持", table
+ *        "量化方案" (int8_w8a16 / int8_w8a8_static) and list "关键设计":
+ *        W8A16 stores INT8 weights and dequantizes to BF16 for a standard
+ *        matmul; W8A8 static calibrates one input_scale per layer offline and
+ *        quantizes activations at run time with that fixed scalar, then runs
+ *        an INT8 GEMM (torch._int_mm).  Calibration size from "快速使用"
+ *        (--calib-samples 64 --calib-seqlen 512).
+ *   The scale granularity (one scale per output channel), the formulas
+ *   scale = max|row|/127 (INT8) and /448 (E4M3), symmetric clamp to
+ *   [-127,127] and the saturating E4M3 cast are the method's stated
+ *   definition of this layer; the pages themselves only name the schemes.
+ *   E4M3 is the OCP 8-bit floating point format "E4M3" (bias 7, 3 mantissa
+ *   bits, no infinities, S.1111.111 is NaN, largest finite 448, subnormal
+ *   step 2^-9).
+ *
+ * Readings where the pages are silent (each is also listed in the design notes):
+ *   - rounding of x/s to an integer is IEEE round-half-to-even (rintf);
+ *   - x/s is one IEEE single-precision division (not a reciprocal multiply);
+ *   - an all-zero row (or calibration batch) gets scale 1.0, so q = 0;
+ *   - the E4M3 cast rounds half-to-even on the E4M3 grid, saturates
+ *     magnitudes beyond 448 to 448 and keeps the sign of zero;
+ *   - W8A16 applies the per-channel scale to the exact k-sum (the scale is a
+ *     per-row constant, so it factors out of the sum); no intermediate BF16
+ *     rounding of s*q;
+ *   - the references below are computed in fp64 (exact for the integer and
+ *     FP8 sums), bias added in fp64; the BF16 cast of the output is left to
+ *     the comparison.
+ *
+ * Every function here has a pin in the not-gpu tests (brute force, closed
+ * forms, invariants, an independent library cast); none is unpinned.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+
+#define ORC_INT8 0
+#define ORC_E4M3 1
+
+/* ---- BF16 storage: the upper 16 bits of an IEEE binary32 ---------------- */
+static float bf16_to_f32(uint16_t h) {
+  uint32_t u = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* ---- OCP E4M3 ------------------------------------------------------------ */
+/* Exact value of an E4M3 code (NaN for S.1111.111).  Normal: 2^(e-7)*(1+m/8)
+ * = (8+m)*2^(e-10); subnormal (e=0): 2^-6*(m/8) = m*2^-9. */
+double orc_e4m3_decode(uint8_t c) {
+  int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return s ? -v : v;
+}
+
+/* Nearest E4M3 code to v, ties to the even mantissa, saturating at +-448,
+ * sign of zero kept.  v is finite (NaN/Inf inputs are outside the contract). */
+uint8_t orc_e4m3_encode(double v) {
+  uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  double a = fabs(v);
+  if (a >= 448.0) return sign | 0x7E;
+  /* binade exponent E = floor(log2 a), held at the subnormal floor -6 */
+  int E = -6;
+  if (a > 0.0) {
+    int e2;
+    frexp(a, &e2); /* a = f*2^e2, f in [0.5,1) */
+    if (e2 - 1 > E) E = e2 - 1;
+  }
+  double quantum = ldexp(1.0, E - 3); /* spacing of the grid in this binade */
+  double r = nearbyint(a / quantum);  /* exact quotient; ties to even integer */
+  double val = r * quantum;           /* r even <=> mantissa field even */
+  if (val == 0.0) return sign;
+  int e2;
+  frexp(val, &e2);
+  int Ev = e2 - 1;
+  if (Ev < -6) return sign | (uint8_t)(val / ldexp(1.0, -9));
+  int mfield = (int)(val / ldexp(1.0, Ev - 3)) - 8;
+  return sign | (uint8_t)(((Ev + 7) << 3) | mfield);
+}
+
+/* ---- one quantization step: q = Q(v), v = fl32(x / s) -------------------- */
+static uint8_t quantize_value(int qtype, float x, float s) {
+  float v = x / s; /* one IEEE binary32 division */
+  if (qtype == ORC_INT8) {
+    float r = rintf(v); /* round half to even */
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    return (uint8_t)(int8_t)(int)r;
+  }
+  return orc_e4m3_encode((double)v);
+}
+
+static float qmax_of(int qtype) { return qtype == ORC_INT8 ? 127.0f : 448.0f; }
+
+/* Per-output-channel symmetric weight quantization of W [N,K] (row-major fp32):
+ * s[n] = fl32(max_k |w[n,k]| / QMAX); q[n,k] = Q(fl32(w[n,k] / s[n])). */
+void orc_quantize_weight(int qtype, int64_t N, int64_t K, const float *w,
+                         uint8_t *q, float *s) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n) {
+    const float *row = w + n * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      float a = fabsf(row[k]);
+      if (a > amax) amax = a;
+    }
+    float sn = (amax > 0.0f) ? amax / qmax_of(qtype) : 1.0f;
+    s[n] = sn;
+    for (int64_t k = 0; k < K; ++k) q[n * K + k] = quantize_value(qtype, row[k], sn);
+  }
+}
+
+/* Static activation scale from a calibration batch x_cal [rows,K] (BF16):
+ * s_x = fl32(max |x_cal| / QMAX), plain abs-max over the whole batch. */
+float orc_act_scale(int qtype, int64_t rows, int64_t K, const uint16_t *x_cal) {
+  float amax = 0.0f;
+#pragma omp parallel for reduction(max : amax) schedule(static)
+  for (int64_t i = 0; i < rows * K; ++i) {
+    float a = fabsf(bf16_to_f32(x_cal[i]));
+    if (a > amax) amax = a;
+  }
+  return (amax > 0.0f) ? amax / qmax_of(qtype) : 1.0f;
+}
+
+/* Static per-tensor activation quantization: q[m,k] = Q(fl32(x[m,k] / s_x)). */
+void orc_quantize_act(int qtype, int64_t M, int64_t K, const uint16_t *x, float s_x,
+                      uint8_t *q) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < M * K; ++i) q[i] = quantize_value(qtype, bf16_to_f32(x[i]), s_x);
+}
+
+/* Exact INT8 GEMM accumulator acc[m,n] = sum_k qx[m,k]*qw[n,k] (int64 sum).
+ * Returns the number of entries that do not fit in int32 (0 for valid inputs:
+ * |acc| <= 127*127*K < 2^31 for K < 133144). */
+int64_t orc_i8_gemm(int64_t M, int64_t K, int64_t N, const int8_t *qx, const int8_t *qw,
+                    int32_t *acc) {
+  int64_t bad = 0;
+#pragma omp parallel for reduction(+ : bad) schedule(static)
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      int64_t a = 0;
+      for (int64_t k = 0; k < K; ++k) a += (int64_t)qx[m * K + k] * (int64_t)qw[n * K + k];
+      if (a > INT32_MAX || a < INT32_MIN) ++bad;
+      acc[m * N + n] = (int32_t)a;
+    }
+  return bad;
+}
+
+static double dequant_code(int qtype, uint8_t c) {
+  return qtype == ORC_INT8 ? (double)(int8_t)c : orc_e4m3_decode(c);
+}
+
+/* Row selection: rows==NULL means all M rows, else y holds nrows output rows. */
+static int64_t pick_row(const int64_t *rows, int64_t i) { return rows ? rows[i] : i; }
+
+/* W8A8 static reference (fp64):
+ *   acc = sum_k deq(qx[m,k]) * deq(qw[n,k])   (exact: int64 for INT8; for E4M3
+ *         every product has <= 8 significant bits inside [2^-18, 2^17.6] and
+ *         the running sum of K < 2^15 of them fits in 53 bits)
+ *   y[m,n] = acc * s_x * s_w[n] + bias[n]. */
+void orc_w8a8(int qtype, int64_t M, int64_t K, int64_t N, const uint8_t *qx, float s_x,
+              const uint8_t *qw, const float *s_w, const uint16_t *bias,
+              const int64_t *rows, int64_t nrows, double *y) {
+  int64_t R = rows ? nrows : M;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t i = 0; i < R; ++i)
+    for (int64_t n = 0; n < N; ++n) {
+      int64_t m = pick_row(rows, i);
+      double acc;
+      if (qtype == ORC_INT8) {
+        int64_t a = 0;
+        for (int64_t k = 0; k < K; ++k)
+          a += (int64_t)(int8_t)qx[m * K + k] * (int64_t)(int8_t)qw[n * K + k];
+        acc = (double)a;
+      } else {
+        acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+          acc += orc_e4m3_decode(qx[m * K + k]) * orc_e4m3_decode(qw[n * K + k]);
+      }
+      double v = acc * (double)s_x * (double)s_w[n];
+      if (bias) v += (double)bf16_to_f32(bias[n]);
+      y[i * N + n] = v;
+    }
+}
+
+/* W8A16 reference (fp64): y[m,n] = s_w[n] * sum_k x[m,k] * deq(q[n,k]) + bias[n],
+ * x in BF16, q the stored 8-bit weight codes. */
+void orc_w8a16(int qtype, int64_t M, int64_t K, int64_t N, const uint16_t *x,
+               const uint8_t *qw, const float *s_w, const uint16_t *bias,
+               const int64_t *rows, int64_t nrows, double *y) {
+  int64_t R = rows ? nrows : M;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t i = 0; i < R; ++i)
+    for (int64_t n = 0; n < N; ++n) {
+      int64_t m = pick_row(rows, i);
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += (double)bf16_to_f32(x[m * K + k]) * dequant_code(qtype, qw[n * K + k]);
+      double v = acc * (double)s_w[n];
+      if (bias) v += (double)bf16_to_f32(bias[n]);
+      y[i * N + n] = v;
+    }
+}
+
+/* Threads the OpenMP runtime will use (1 when built without OpenMP). */
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
