@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the 8-bit quantized linear (libqlin, C ABI).
+
+A step is one pass over a workload's linears with inputs resident in HBM.  The
+default workload is the FP8-E4M3 W8A16 decode sweep on 7B-class shapes
+(q_proj 3584->3584, gate_up_proj 3584->37888, down_proj 18944->3584, each at
+M in {1, 8, 32, 128, 256}); the metric is quantized-linear GB/s of algorithmic
+bytes (8-bit weights + fp32 scales + BF16 activations in + BF16 outputs out).
+Two copies of the weights (2 x 217 MB, each larger than the 129 MB L2)
+alternate between steps, so every step streams its weights from HBM.
+
+Other workloads (--workload): small, w8a8-3b, prefill, stack-decode,
+stack-prefill; prefill-shaped ones report TFLOP/s instead of GB/s.
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the layer)
+on a bounded sample of the same workload on the host cores.
+
+Under torchrun (--gpus N > 1) every rank runs an independent replica (the layer
+has no exchange step); value is the sum over ranks of units / max elapsed.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_quantized_linear_gb300 import synth  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- workloads
+def workload_calls(name: str):
+    """List of synth.Linear describing one step of the workload."""
+    if name == "decode7b":
+        return synth.workload(synth.DECODE7B).linears, synth.DECODE7B
+    if name == "small":
+        return synth.workload(synth.SMALL).linears, synth.SMALL
+    if name == "w8a8-3b":
+        return synth.workload(synth.W8A8_3B).linears, synth.W8A8_3B
+    if name == "prefill":
+        return synth.workload(synth.PREFILL).linears, synth.PREFILL
+    if name == "stack-decode":
+        return synth.stack_linears("decode"), synth.STACK + "-decode"
+    if name == "stack-prefill":
+        return synth.stack_linears("prefill"), synth.STACK + "-prefill"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def alg_bytes(l) -> int:
+    b = l.N * l.K + 4 * l.N + 2 * l.M * l.K + 2 * l.M * l.N
+    if l.bias:
+        b += 2 * l.N
+    return b
+
+
+def alg_flops(l) -> int:
+    return 2 * l.M * l.N * l.K
+
+
+def is_prefill(name: str) -> bool:
+    return name in ("prefill", "stack-prefill")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ----------------------------------------------------------- GPU workload
+class GpuWorkload:
+    """Quantized weights, inputs and pre-marshalled C-ABI arguments of one step."""
+
+    def __init__(self, name, dev, copies=2):
+        import torch
+        from bit_quantized_linear_gb300 import capi
+        self.torch, self.capi = torch, capi
+        self.lins, self.wl = workload_calls(name)
+        self.name = name
+        self.dev = dev
+        L = capi.lib()
+        self.stream = torch.cuda.current_stream()
+        sp = ctypes.c_void_p(self.stream.cuda_stream)
+        # weights: one quantized copy per distinct (layer, name, K, N, qtype), then `copies` sets
+        wkeys = {}
+        for l in self.lins:
+            wkeys.setdefault((l.workload, l.layer, l.name, l.K, l.N, l.qtype), l)
+        self.weight_bytes = sum(l.N * l.K for l in wkeys.values())
+        self.copies = copies if self.weight_bytes < 4 * L2_BYTES else 1
+        self.wsets = [dict() for _ in range(self.copies)]
+        self.scales = {}
+        for key, l in wkeys.items():
+            w = torch.from_numpy(synth.make_inputs(l, want=("w",))["w"]).to(dev)
+            qw, s = capi.quantize_weight(l.qtype, w)
+            del w
+            self.scales[key] = s
+            self.wsets[0][key] = qw
+            for c in range(1, self.copies):
+                self.wsets[c][key] = qw.clone()
+        # activations, calibration scales, bias, outputs
+        self.x, self.y, self.bias, self.sx, self.ws = [], [], [], [], []
+        self.x_host, self.y_host = [], []
+        cache = {}
+        for l in self.lins:
+            k = (l.workload, l.layer, l.name, l.K, l.M)
+            if k not in cache:
+                t = synth.make_inputs(l, want=("x", "cal", "bias"))
+                cache[k] = t
+            t = cache[k]
+            xt = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+            self.x.append(xt)
+            self.x_host.append(torch.from_numpy(t["x"].view(np.int16)).view(torch.bfloat16).pin_memory())
+            self.y.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
+            self.y_host.append(torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory())
+            self.bias.append(torch.from_numpy(t["bias"].view(np.int16)).to(dev).view(torch.bfloat16)
+                             if "bias" in t else None)
+            if l.form == "w8a8":
+                cal = torch.from_numpy(t["cal"].view(np.int16)).to(dev).view(torch.bfloat16)
+                self.sx.append(capi.act_scale_from_calib(l.qtype, cal))
+                del cal
+                self.ws.append(capi.workspace(capi.QLIN_OP_W8A8_LINEAR, l.qtype, l.M, l.K, l.N, device=dev))
+            else:
+                self.sx.append(None)
+                self.ws.append(capi.workspace(capi.QLIN_OP_W8A16_LINEAR, l.qtype, l.M, l.K, l.N, device=dev))
+            if len(cache) > 8:
+                cache.clear()
+        torch.cuda.synchronize()
+        P = ctypes.c_void_p
+
+        def ptr(t):
+            return None if t is None else P(t.data_ptr())
+
+        # pre-marshalled argument tuples: args[copy][i]
+        self.fns, self.args = [], [[] for _ in range(self.copies)]
+        for i, l in enumerate(self.lins):
+            key = (l.workload, l.layer, l.name, l.K, l.N, l.qtype)
+            qt = capi.QTYPES[l.qtype]
+            ws = self.ws[i]
+            wsp, wsb = (None, 0) if ws is None else (ptr(ws), ws.numel())
+            if l.form == "w8a16":
+                self.fns.append(L.qlin_w8a16_linear)
+                for c in range(self.copies):
+                    self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.wsets[c][key]),
+                                         ptr(self.scales[key]), ptr(self.bias[i]), ptr(self.y[i]), wsp, wsb, sp))
+            else:
+                self.fns.append(L.qlin_w8a8_linear)
+                for c in range(self.copies):
+                    self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.sx[i]),
+                                         ptr(self.wsets[c][key]), ptr(self.scales[key]), ptr(self.bias[i]),
+                                         ptr(self.y[i]), wsp, wsb, sp))
+        op = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR}
+        self.kernel = [capi.qlin_kernel_name(op[l.form], l.qtype, l.M, l.K, l.N) for l in self.lins]
+
+    def run_step(self, step, ev=None):
+        args = self.args[step % self.copies]
+        for i, fn in enumerate(self.fns):
+            if ev is not None:
+                ev[i][0].record(self.stream)
+            st = fn(*args[i])
+            if ev is not None:
+                ev[i][1].record(self.stream)
+            if st != 0:
+                raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
+
+    def run_step_e2e(self, step):
+        for i in range(len(self.lins)):
+            self.x[i].copy_(self.x_host[i], non_blocking=True)
+        self.run_step(step)
+        for i in range(len(self.lins)):
+            self.y_host[i].copy_(self.y[i], non_blocking=True)
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "bit_quantized_linear_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, wl: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{wl}:{kernel}")
+    if not e or e.get("kernel_digest") != kernel_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU side
+def oracle_sample(name, rows_per_call=1):
+    """Bounded oracle sample of one step: every linear of the workload, first
+    `rows_per_call` output rows (the oracle still streams the whole weight)."""
+    import oracle
+    lins, wl = workload_calls(name)
+    if name.startswith("stack"):
+        lins = lins[:6]  # one layer of the stack
+    prepared = []
+    for l in lins:
+        t = synth.make_inputs(l, want=("w", "cal", "bias"))
+        qt = oracle.INT8 if l.qtype == "int8" else oracle.E4M3
+        q, s = oracle.quantize_weight(qt, t["w"])
+        r = min(l.M, rows_per_call)
+        # the first r rows of the workload's activations (the generator draws rows in order)
+        x = synth.make_inputs(l, want=("x",), x_rows=r)["x"]
+        sx = oracle.act_scale(qt, t["cal"]) if l.form == "w8a8" else None
+        sub = synth.Linear(l.name, l.K, l.N, r, l.qtype, l.form, l.bias, l.outliers, l.workload, l.layer)
+        prepared.append((l, sub, qt, q, s, x, sx, t.get("bias")))
+
+    def run():
+        for l, sub, qt, q, s, x, sx, b in prepared:
+            if l.form == "w8a16":
+                oracle.w8a16(qt, x, q, s, b)
+            else:
+                qx = oracle.quantize_act(qt, x, sx)
+                oracle.w8a8(qt, qx, sx, q, s, b)
+
+    units = sum(alg_flops(p[1]) if is_prefill(name) else alg_bytes(p[1]) for p in prepared)
+    desc = (f"{len(prepared)} linears of the workload, first {rows_per_call} output row(s) each "
+            f"(the oracle streams every weight once per row)")
+    return run, units, desc, oracle.num_threads()
+
+
+def cpu_baseline(name, unit_scale, unit):
+    run, units, desc, cores = oracle_sample(name)
+    run()  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 > 10.0 or n >= 20:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": units / dt / unit_scale, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": desc + f"; {n} timed repetitions, {dt:.3f} s each"}
+
+
+# ------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
+    ap.add_argument("--workload", default="decode7b",
+                    choices=["decode7b", "small", "w8a8-3b", "prefill", "stack-decode", "stack-prefill"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        a.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    prefill = is_prefill(a.workload)
+    metric_unit = "TFLOP/s" if prefill else "GB/s"
+    metric = ("quantized-linear TOPS (prefill), % of roofline" if prefill
+              else "quantized-linear GB/s (decode M<=256), % of roofline")
+    lins, wl = workload_calls(a.workload)
+    unit_scale = 1e12 if prefill else 1e9
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        run, units, desc, cores = oracle_sample(a.workload)
+        for _ in range(a.warmup):
+            run()
+        t0 = time.perf_counter()
+        for _ in range(a.steps):
+            run()
+        dt = (time.perf_counter() - t0) / a.steps
+        v = units / dt / unit_scale
+        print(json.dumps({
+            "impl": "reference", "metric": metric, "value": v, "unit": metric_unit, "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl, "sample": desc},
+            "cpu_baseline": {"value": v, "unit": metric_unit, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": metric_unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bit_quantized_linear_gb300 import capi
+
+    W = GpuWorkload(a.workload, dev)
+    n = len(W.lins)
+    units_step = sum(alg_flops(l) if prefill else alg_bytes(l) for l in W.lins)
+    bytes_step = sum(alg_bytes(l) for l in W.lins)
+    flops_step = sum(alg_flops(l) for l in W.lins)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for s in range(a.warmup):
+        W.run_step(s)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region (inputs resident) ----
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n)]
+           for _ in range(a.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = capi.qlin_launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(W.stream)
+        for s in range(a.steps):
+            W.run_step(s, evs[s])
+        t_end.record(W.stream)
+        torch.cuda.synchronize()
+        barrier()
+    launches = capi.qlin_launch_count() - launches0
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    clocks = clk.summary()
+    if torch.cuda.get_device_properties(dev).name and clocks.get("reasons") is None:
+        clocks["reasons"] = []
+    ms_step = elapsed / a.steps * 1e3
+    value = units_step * a.steps * world / elapsed / unit_scale
+
+    # per-call durations -> per-kernel attribution
+    dur = np.array([[evs[s][i][0].elapsed_time(evs[s][i][1]) / 1e3 for i in range(n)] for s in range(a.steps)])
+    mean_call = dur.mean(axis=0)
+    per_kernel = {}
+    for i, l in enumerate(W.lins):
+        k = W.kernel[i]
+        d = per_kernel.setdefault(k, {"time": 0.0, "bytes": 0, "flops": 0, "calls": 0})
+        d["time"] += mean_call[i]
+        d["bytes"] += alg_bytes(l)
+        d["flops"] += alg_flops(l)
+        d["calls"] += 1
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["time"])
+    peaks, peaks_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    bf16 = peaks["bf16_tflops"]
+    d = per_kernel[dom]
+    if prefill:
+        # FP8 operands: measured BF16 peak x the nominal FP8/BF16 ratio (4.5 / 2.25)
+        peak = bf16 * 2.0 if W.lins[0].qtype == "e4m3" else bf16
+        roof = {"bound": "tensor", "achieved": d["flops"] / d["time"] / 1e12, "peak": peak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": d["bytes"] / d["time"] / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = traffic_for(dom.split("+")[-1], wl)
+    roof["traffic"] = tr
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured" else "fallback"
+    # roofline time over the whole step: sum_i max(bytes_i / BW, flops_i / peak_i) / measured
+    rt = 0.0
+    for l in W.lins:
+        tpk = (bf16 * 2.0 if (l.form == "w8a8" and l.qtype == "e4m3") else bf16) * 1e12
+        rt += max(alg_bytes(l) / (hbm * 1e9), alg_flops(l) / tpk)
+    roof["step_roofline_time_frac"] = rt / (mean_call.sum())
+    calls = []
+    for i, l in enumerate(W.lins):
+        calls.append({"name": l.name, "M": l.M, "K": l.K, "N": l.N, "kernel": W.kernel[i],
+                      "us": round(mean_call[i] * 1e6, 2),
+                      "GB/s": round(alg_bytes(l) / mean_call[i] / 1e9, 1),
+                      "TFLOP/s": round(alg_flops(l) / mean_call[i] / 1e12, 1)})
+
+    # ---- end-to-end through the C ABI with host buffers ----
+    e2e = None
+    if not a.no_e2e:
+        for s in range(a.warmup):
+            W.run_step_e2e(s)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(W.stream)
+        for s in range(a.steps):
+            W.run_step_e2e(s)
+        e1.record(W.stream)
+        torch.cuda.synchronize()
+        et = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([et], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            et = float(t.item())
+        e2e = {"value": units_step * a.steps * world / et / unit_scale, "unit": metric_unit,
+               "h2d_bytes_per_step": int(sum(2 * l.M * l.K for l in W.lins)),
+               "d2h_bytes_per_step": int(sum(2 * l.M * l.N for l in W.lins))}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_baseline(a.workload, unit_scale, metric_unit)
+
+    if rank == 0:
+        out = {
+            "metric": metric, "value": value, "unit": metric_unit, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": ("e4m3" if W.lins[0].qtype == "e4m3" else "int8") + ("xbf16" if W.lins[0].form == "w8a16" else "")
+                     + "->f32acc->bf16",
+            "data": "synthetic",
+            "config": {"workload": wl, "linears": n, "bytes_per_step": bytes_step, "flops_per_step": flops_step,
+                       "weight_bytes": W.weight_bytes, "weight_copies": W.copies,
+                       "l2": (f"{W.copies} alternating weight copies of {W.weight_bytes / 1e6:.0f} MB each "
+                              f"(L2 is {L2_BYTES / 2**20:.0f} MiB)"),
+                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "calls": calls,
+        }
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,49 @@
+// Internal launcher declarations shared by the C-ABI shim and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qlin {
+
+struct DeviceInfo {
+  int device = -1;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  unsigned *status = nullptr;  // device status word (QLIN_ERR_TIMEOUT on a run-out wait)
+};
+
+// Host-side count of kernels enqueued by the library (qlin_launch_count).
+void note_launches(int n);
+
+cudaError_t launch_quantize_weight(int qtype, int64_t N, int64_t K, const float *w, void *qw,
+                                   float *s, cudaStream_t st);
+cudaError_t launch_act_scale(int qtype, int64_t rows, int64_t K, const void *x, float *scale,
+                             void *ws, int sms, cudaStream_t st);
+cudaError_t launch_quantize_act(int qtype, int64_t M, int64_t K, const void *x, const float *s,
+                                void *qx, int sms, cudaStream_t st);
+
+// GEMM epilogue / operand modes.
+enum GemmMode {
+  kW8A16 = 0,   // A = BF16 x, B = 8-bit weight codes, acc fp32, y = acc*s_w[n] + b
+  kW8A8 = 1,    // A = 8-bit activation codes, B = 8-bit weight codes, y = acc*(s_x*s_w[n]) + b
+  kI8Raw = 2    // INT8 codes, raw int32 accumulator out
+};
+
+struct GemmArgs {
+  int mode;
+  int qtype;
+  int64_t M, K, N;
+  const void *a;          // x (BF16) or qx (codes)
+  const void *qw;         // [N,K] codes
+  const float *w_scale;   // [N]
+  const float *x_scale;   // device scalar (kW8A8) or null
+  const uint16_t *bias;   // [N] or null
+  void *y;                // [M,N] BF16, or int32 for kI8Raw
+};
+
+cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
+
+cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
+                              cudaStream_t st);
+
+}  // namespace qlin

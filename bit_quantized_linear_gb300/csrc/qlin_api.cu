@@ -1,0 +1,215 @@
+// C-ABI shim of libqlin: argument validation, workspace sizing, kernel choice
+// by shape, and launches on the caller's stream.  No entry point allocates
+// device memory or throws; every failure is a qlin_status.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qlin {
+
+// Device status word (one per device context); set by bounded device waits.
+__device__ unsigned g_device_status = 0;
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static constexpr int kMaxDevices = 64;
+static DeviceInfo g_dev[kMaxDevices];
+static std::mutex g_dev_mu;
+
+// Caches the SM count, compute capability and status-word address of the
+// current device.  Returns QLIN_OK or an error status.
+static qlin_status current_device(DeviceInfo **out) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return QLIN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo &di = g_dev[d];
+  if (di.device != d) {
+    DeviceInfo t;
+    t.device = d;
+    if (cudaDeviceGetAttribute(&t.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.cc_major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.cc_minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess)
+      return QLIN_ERR_CUDA;
+    if (t.cc_major != 10 || t.cc_minor != 3) return QLIN_ERR_UNSUPPORTED;  // built for sm_103a only
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return QLIN_ERR_CUDA;
+    t.status = (unsigned *)p;
+    di = t;
+  }
+  *out = &di;
+  return QLIN_OK;
+}
+
+static inline bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static inline bool valid_qtype(int t) { return t == QLIN_INT8 || t == QLIN_E4M3; }
+static inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+static inline qlin_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+
+// Common shape checks of the linear entry points.
+static qlin_status check_linear_shape(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K < 16 || N < 16 || (K % 16) || (N % 16)) return QLIN_ERR_INVALID_ARG;
+  if (M > (int64_t)1 << 31 || K > (int64_t)1 << 17 || N > (int64_t)1 << 31) return QLIN_ERR_INVALID_ARG;
+  return QLIN_OK;
+}
+
+}  // namespace qlin
+
+using namespace qlin;
+
+extern "C" {
+
+int qlin_version(void) { return 100; }
+
+uint64_t qlin_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, int64_t N) {
+  if (!valid_qtype(qtype)) return "invalid";
+  switch (op) {
+    case QLIN_OP_QUANTIZE_WEIGHT: return "k_quantize_weight";
+    case QLIN_OP_ACT_SCALE: return "k_absmax_bf16+k_scale_finalize";
+    case QLIN_OP_QUANTIZE_ACT: return "k_quantize_act";
+    case QLIN_OP_W8A16_LINEAR:
+    case QLIN_OP_I8_GEMM_S32:
+      if (check_linear_shape(M, K, N)) return "invalid";
+      return M == 0 ? "none" : "k_gemm_simt";
+    case QLIN_OP_W8A8_LINEAR:
+      if (check_linear_shape(M, K, N)) return "invalid";
+      return M == 0 ? "none" : "k_quantize_act+k_gemm_simt";
+  }
+  return "invalid";
+}
+
+const char *qlin_status_string(qlin_status s) {
+  switch (s) {
+    case QLIN_OK: return "QLIN_OK";
+    case QLIN_ERR_INVALID_ARG: return "QLIN_ERR_INVALID_ARG";
+    case QLIN_ERR_UNSUPPORTED: return "QLIN_ERR_UNSUPPORTED";
+    case QLIN_ERR_WORKSPACE: return "QLIN_ERR_WORKSPACE";
+    case QLIN_ERR_CUDA: return "QLIN_ERR_CUDA";
+    case QLIN_ERR_TIMEOUT: return "QLIN_ERR_TIMEOUT";
+  }
+  return "QLIN_ERR_UNKNOWN";
+}
+
+size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, int64_t N) {
+  if (!valid_qtype(qtype) || M < 0 || K < 0 || N < 0) return (size_t)-1;
+  switch (op) {
+    case QLIN_OP_QUANTIZE_WEIGHT: return 0;
+    case QLIN_OP_ACT_SCALE: return 256;
+    case QLIN_OP_QUANTIZE_ACT: return 0;
+    case QLIN_OP_W8A16_LINEAR: return 0;
+    case QLIN_OP_W8A8_LINEAR: return round_up((size_t)M * (size_t)K, 256);
+    case QLIN_OP_I8_GEMM_S32: return 0;
+  }
+  return (size_t)-1;
+}
+
+qlin_status qlin_quantize_weight(qlin_qtype qtype, int64_t N, int64_t K, const float *w, void *qw,
+                                 float *w_scale, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (N < 0 || K < 16 || (K % 16) || N > ((int64_t)1 << 31) - 1) return QLIN_ERR_INVALID_ARG;
+  if (!w || !qw || !w_scale || !al16(w) || !al16(qw) || !al16(w_scale)) return QLIN_ERR_INVALID_ARG;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  return from_cuda(launch_quantize_weight(qtype, N, K, w, qw, w_scale, (cudaStream_t)stream));
+}
+
+qlin_status qlin_act_scale_from_calib(qlin_qtype qtype, int64_t rows, int64_t K, const void *x_cal,
+                                      float *input_scale, void *ws, size_t ws_bytes,
+                                      qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (rows < 1 || K < 16 || (K % 16)) return QLIN_ERR_INVALID_ARG;
+  if (!x_cal || !input_scale || !al16(x_cal) || !al16(input_scale)) return QLIN_ERR_INVALID_ARG;
+  if (!ws || !al16(ws) || ws_bytes < qlin_workspace_bytes(QLIN_OP_ACT_SCALE, qtype, rows, K, 0))
+    return QLIN_ERR_WORKSPACE;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  return from_cuda(launch_act_scale(qtype, rows, K, x_cal, input_scale, ws, dev->sms,
+                                    (cudaStream_t)stream));
+}
+
+qlin_status qlin_quantize_act_static(qlin_qtype qtype, int64_t M, int64_t K, const void *x,
+                                     const float *input_scale, void *qx, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (M < 0 || K < 16 || (K % 16)) return QLIN_ERR_INVALID_ARG;
+  if (!x || !input_scale || !qx || !al16(x) || !al16(qx) || ((uintptr_t)input_scale & 3u))
+    return QLIN_ERR_INVALID_ARG;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  return from_cuda(launch_quantize_act(qtype, M, K, x, input_scale, qx, dev->sms, (cudaStream_t)stream));
+}
+
+qlin_status qlin_w8a16_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                              const void *qw, const float *w_scale, const void *bias, void *y,
+                              void *ws, size_t ws_bytes, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = check_linear_shape(M, K, N)) return s;
+  if (!x || !qw || !w_scale || !y || !al16(x) || !al16(qw) || !al16(w_scale) || !al16(y) ||
+      (bias && !al16(bias)))
+    return QLIN_ERR_INVALID_ARG;
+  const size_t need = qlin_workspace_bytes(QLIN_OP_W8A16_LINEAR, qtype, M, K, N);
+  if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  GemmArgs g{kW8A16, qtype, M, K, N, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
+  return from_cuda(launch_gemm_simt(g, *dev, (cudaStream_t)stream));
+}
+
+qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                             const float *input_scale, const void *qw, const float *w_scale,
+                             const void *bias, void *y, void *ws, size_t ws_bytes,
+                             qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = check_linear_shape(M, K, N)) return s;
+  if (!x || !input_scale || !qw || !w_scale || !y || !al16(x) || !al16(qw) || !al16(w_scale) ||
+      !al16(y) || (bias && !al16(bias)) || ((uintptr_t)input_scale & 3u))
+    return QLIN_ERR_INVALID_ARG;
+  const size_t need = qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N);
+  if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaError_t e = launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st)) return QLIN_ERR_CUDA;
+  GemmArgs g{kW8A8, qtype, M, K, N, ws, qw, w_scale, input_scale, (const uint16_t *)bias, y};
+  return from_cuda(launch_gemm_simt(g, *dev, st));
+}
+
+qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, const void *qw,
+                             int32_t *acc, void *ws, size_t ws_bytes, qlin_stream_t stream) {
+  if (qlin_status s = check_linear_shape(M, K, N)) return s;
+  if (!qx || !qw || !acc || !al16(qx) || !al16(qw) || !al16(acc)) return QLIN_ERR_INVALID_ARG;
+  const size_t need = qlin_workspace_bytes(QLIN_OP_I8_GEMM_S32, QLIN_INT8, M, K, N);
+  if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  GemmArgs g{kI8Raw, QLIN_INT8, M, K, N, qx, qw, nullptr, nullptr, nullptr, acc};
+  return from_cuda(launch_gemm_simt(g, *dev, (cudaStream_t)stream));
+}
+
+qlin_status qlin_get_device_status(qlin_stream_t stream) {
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return QLIN_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QLIN_ERR_CUDA;
+  if (v && cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return QLIN_ERR_CUDA;
+  return v ? (qlin_status)v : QLIN_OK;
+}
+
+qlin_status qlin_debug_wait_flag(const uint32_t *flag, uint64_t timeout_ns, qlin_stream_t stream) {
+  if (!flag || ((uintptr_t)flag & 3u)) return QLIN_ERR_INVALID_ARG;
+  if (timeout_ns > 1000000000ull) timeout_ns = 1000000000ull;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  return from_cuda(launch_debug_wait(flag, timeout_ns, dev->status, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+// Quantizers: per-output-channel weight quantization, calibration abs-max and
+// static per-tensor activation quantization.  All HBM-streaming kernels with
+// 16-byte vector accesses; the arithmetic of one element is qlin::quantize_one.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qlin {
+
+// ---------------------------------------------------------------------------
+// Weight quantization: one CTA per output row n.
+//   pass 1: s = max_k |w[n,k]| / QMAX (s = 1 for an all-zero row)
+//   pass 2: q[n,k] = Q(w[n,k] / s), 16 codes (one 16-byte store) per step.
+// The second pass re-reads the row, which is at most 76 KB and served by L2.
+// ---------------------------------------------------------------------------
+template <int QT>
+__global__ void __launch_bounds__(256) k_quantize_weight(const float *__restrict__ w,
+                                                         uint8_t *__restrict__ q,
+                                                         float *__restrict__ s, int64_t K) {
+  __shared__ float red[8];
+  const int64_t n = blockIdx.x;
+  const float4 *row = reinterpret_cast<const float4 *>(w + n * K);
+  const int64_t K16 = K / 16;
+  float amax = 0.0f;
+  for (int64_t i = threadIdx.x; i < K / 4; i += blockDim.x) {
+    float4 v = __ldg(row + i);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+  const float sc = amax > 0.0f ? __fdiv_rn(amax, qmax_of(QT)) : 1.0f;
+  if (threadIdx.x == 0) s[n] = sc;
+  uint4 *qrow = reinterpret_cast<uint4 *>(q + n * K);
+  for (int64_t i = threadIdx.x; i < K16; i += blockDim.x) {
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float4 v = __ldg(row + 4 * i + j);
+      out[j] = (uint32_t)quantize_one<QT>(v.x, sc) | ((uint32_t)quantize_one<QT>(v.y, sc) << 8) |
+               ((uint32_t)quantize_one<QT>(v.z, sc) << 16) |
+               ((uint32_t)quantize_one<QT>(v.w, sc) << 24);
+    }
+    qrow[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Calibration abs-max: grid-stride over 8-element BF16 chunks, CTA reduction,
+// then one atomicMax on the fp32 bit pattern (non-negative floats order like
+// their bit patterns).  The finalize kernel turns it into the scale.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_absmax_bf16(const uint4 *__restrict__ x, int64_t n8,
+                                                     unsigned *__restrict__ out) {
+  __shared__ float red[8];
+  float amax = 0.0f;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 v = __ldg(x + i);
+    uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // |bf16| for both halves: clear the sign bits, then compare as floats.
+      amax = fmaxf(amax, __uint_as_float((wds[j] & 0x7FFFu) << 16));
+      amax = fmaxf(amax, __uint_as_float(wds[j] & 0x7FFF0000u));
+    }
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+    amax = fmaxf(amax, red[0]);
+    atomicMax(out, __float_as_uint(amax));
+  }
+}
+
+__global__ void k_scale_finalize(const unsigned *__restrict__ amax_bits, float *__restrict__ scale,
+                                 float qmax) {
+  const float a = __uint_as_float(*amax_bits);
+  *scale = a > 0.0f ? __fdiv_rn(a, qmax) : 1.0f;
+}
+
+// ---------------------------------------------------------------------------
+// Static activation quantization: 16 BF16 in (two 16-byte loads), 16 codes out
+// (one 16-byte store) per thread step.  The scale is read from device memory.
+// ---------------------------------------------------------------------------
+template <int QT>
+__global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ x,
+                                                      const float *__restrict__ s_ptr,
+                                                      uint4 *__restrict__ q, int64_t n16) {
+  const float s = __ldg(s_ptr);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 a = __ldg(x + 2 * i), b = __ldg(x + 2 * i + 1);
+    uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t lo = in[2 * j], hi = in[2 * j + 1];
+      out[j] = (uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo & 0xFFFFu), s) |
+               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo >> 16), s) << 8) |
+               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi & 0xFFFFu), s) << 16) |
+               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi >> 16), s) << 24);
+    }
+    q[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// --------------------------------- launchers --------------------------------
+static int stream_grid(int64_t work, int per_cta, int sms) {
+  int64_t g = (work + per_cta - 1) / per_cta;
+  int64_t cap = (int64_t)sms * 8;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_quantize_weight(int qtype, int64_t N, int64_t K, const float *w, void *qw,
+                                   float *s, cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  dim3 grid((unsigned)N), block(256);
+  if (qtype == QLIN_INT8)
+    k_quantize_weight<QLIN_INT8><<<grid, block, 0, st>>>(w, (uint8_t *)qw, s, K);
+  else
+    k_quantize_weight<QLIN_E4M3><<<grid, block, 0, st>>>(w, (uint8_t *)qw, s, K);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_scale(int qtype, int64_t rows, int64_t K, const void *x, float *scale,
+                             void *ws, int sms, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  const int64_t n8 = rows * K / 8;
+  k_absmax_bf16<<<stream_grid(n8, 256 * 4, sms), 256, 0, st>>>((const uint4 *)x, n8, (unsigned *)ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_scale_finalize<<<1, 1, 0, st>>>((const unsigned *)ws, scale, qmax_of(qtype));
+  note_launches(2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_act(int qtype, int64_t M, int64_t K, const void *x, const float *s,
+                                void *qx, int sms, cudaStream_t st) {
+  const int64_t n16 = M * K / 16;
+  if (n16 == 0) return cudaSuccess;
+  const int grid = stream_grid(n16, 256, sms);
+  if (qtype == QLIN_INT8)
+    k_quantize_act<QLIN_INT8><<<grid, 256, 0, st>>>((const uint4 *)x, s, (uint4 *)qx, n16);
+  else
+    k_quantize_act<QLIN_E4M3><<<grid, 256, 0, st>>>((const uint4 *)x, s, (uint4 *)qx, n16);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace qlin

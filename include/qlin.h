@@ -1,0 +1,206 @@
+/*
+ * qlin.h -- C ABI of libqlin, an 8-bit quantized linear layer for GB300 (sm_103a).
+ *
+ * Two forms of the layer, as the serving pages describe them:
+ *   W8A16 weight-only: 8-bit weights (INT8 or OCP FP8-E4M3) with one scale per
+ *     output channel, BF16 activations; the weights are dequantized to BF16 and
+ *     a standard matmul with fp32 accumulation follows ("Nano-vLLM-MoE" README,
+ *     "FP8 W8A16 weight-only quantization", Setup; "Nano-vLLM-MOE" README,
+ *     "INT8 量化支持", list "关键设计", W8A16 item).
+ *   W8A8 static: activations are quantized with one offline-calibrated
+ *     per-tensor input_scale, then an 8-bit GEMM runs with a scale epilogue
+ *     ("Nano-vLLM-MOE" README, "INT8 量化支持", "关键设计", W8A8 static item;
+ *     "Nano-vLLM-MoE" README, "FP8 W8A8 static quantization", Setup:
+ *     offline-calibrated activation scales, linear backends with a custom
+ *     epilogue).
+ * The per-output-channel granularity, scale = max|row|/127 (INT8) or /448
+ * (E4M3), the symmetric clamp to [-127,127] and the saturating E4M3 cast are
+ * this layer's stated definition; the pages only name the schemes.
+ *
+ * Conventions for every entry point:
+ *   - Layouts are row-major and dense: x [M,K] BF16, W / qw [N,K] (nn.Linear,
+ *     K contiguous), y [M,N] BF16, w_scale [N] fp32, bias [N] BF16.
+ *     BF16 data is passed as raw 16-bit patterns (uint16_t storage).
+ *   - All data pointers are DEVICE pointers into memory the caller owns.  The
+ *     library allocates no device memory on these paths; where an operation
+ *     needs scratch it takes a caller-owned workspace (`ws`, `ws_bytes`) whose
+ *     size qlin_workspace_bytes() reports.  Nothing is retained between calls.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream) and
+ *     returns once the work is enqueued.  Only qlin_get_device_status()
+ *     synchronizes.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     returned as a status: NULL required pointer, negative sizes, K or N not a
+ *     multiple of 16, pointers not 16-byte aligned, unknown qtype, workspace
+ *     too small.  A CUDA launch error is returned as QLIN_ERR_CUDA.  No entry
+ *     point aborts, traps or throws across the ABI.
+ *   - M == 0 is valid and enqueues nothing.
+ *   - Device-side waits in the kernels are bounded; a wait that runs out sets
+ *     a device status word instead of hanging, which qlin_get_device_status()
+ *     reports as QLIN_ERR_TIMEOUT.
+ */
+#ifndef QLIN_H_
+#define QLIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st *qlin_stream_t;
+
+typedef enum {
+  QLIN_OK = 0,
+  QLIN_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misalignment, K/N % 16 != 0 */
+  QLIN_ERR_UNSUPPORTED = 2, /* no device, not sm_103, or qtype not valid here */
+  QLIN_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes < qlin_workspace_bytes() */
+  QLIN_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  QLIN_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (device status) */
+} qlin_status;
+
+typedef enum {
+  QLIN_INT8 = 0, /* signed 8-bit integer codes in [-127, 127] */
+  QLIN_E4M3 = 1  /* OCP FP8 E4M3 ("e4m3fn"): bias 7, no inf, max finite 448 */
+} qlin_qtype;
+
+typedef enum {
+  QLIN_OP_QUANTIZE_WEIGHT = 0,
+  QLIN_OP_ACT_SCALE = 1,
+  QLIN_OP_QUANTIZE_ACT = 2,
+  QLIN_OP_W8A16_LINEAR = 3,
+  QLIN_OP_W8A8_LINEAR = 4,
+  QLIN_OP_I8_GEMM_S32 = 5
+} qlin_op;
+
+/*
+ * Per-output-channel symmetric weight quantization (offline export step;
+ * "Nano-vLLM-MOE" README, "INT8 量化支持", 快速使用 step 1 `--scheme int8_w8a16`;
+ * "Nano-vLLM-MoE" README, FP8 W8A16 Setup, `--scheme fp8_w8a16` export).
+ *   w        [N,K] fp32 input weights (device, read only).
+ *   qw       [N,K] 1-byte output codes (device): int8 two's complement for
+ *            QLIN_INT8, E4M3 bit patterns for QLIN_E4M3.
+ *   w_scale  [N] fp32 output scales (device).
+ * Computes, per row n:  s = max_k |w[n,k]| / QMAX  (QMAX = 127 or 448, one IEEE
+ * binary32 division; s = 1 for an all-zero row), then for every k
+ *   v = w[n,k] / s (IEEE binary32 division) and
+ *   INT8: q = clamp(round_half_even(v), -127, 127);
+ *   E4M3: q = nearest E4M3 value (ties to even), |v| > 448 saturates to +-448.
+ * Requirements: N >= 0, K >= 16, K % 16 == 0, all pointers 16-byte aligned.
+ */
+qlin_status qlin_quantize_weight(qlin_qtype qtype, int64_t N, int64_t K, const float *w,
+                                 void *qw, float *w_scale, qlin_stream_t stream);
+
+/*
+ * Static per-tensor activation scale from a calibration batch (offline
+ * calibration; "Nano-vLLM-MOE" README, "INT8 量化支持", 关键设计 W8A8 static
+ * item: offline per-layer input_scale; 快速使用 step 2:
+ * `--calib-samples 64 --calib-seqlen 512`).
+ *   x_cal        [rows,K] BF16 calibration activations (device).
+ *   input_scale  one fp32 output on the device: max|x_cal| / QMAX, or 1 when the
+ *                batch is all zero.
+ *   ws           device workspace of qlin_workspace_bytes(QLIN_OP_ACT_SCALE, ...)
+ *                bytes (4 bytes today, 256-byte aligned); overwritten.
+ * Requirements: rows >= 1, K >= 16, K % 16 == 0, pointers 16-byte aligned.
+ */
+qlin_status qlin_act_scale_from_calib(qlin_qtype qtype, int64_t rows, int64_t K,
+                                      const void *x_cal, float *input_scale, void *ws,
+                                      size_t ws_bytes, qlin_stream_t stream);
+
+/*
+ * Static activation quantization with the fixed calibrated scalar
+ * ("Nano-vLLM-MOE" README, "INT8 量化支持", 关键设计 W8A8 static item:
+ * quantize activations at run time with the fixed scalar).
+ *   x            [M,K] BF16 (device).
+ *   input_scale  one fp32 on the device (so the call can sit in a CUDA graph).
+ *   qx           [M,K] 1-byte output codes (device):
+ *                INT8: clamp(round_half_even(x / s), -127, 127)
+ *                E4M3: saturating round-half-even E4M3 cast of x / s.
+ * Requirements: M >= 0, K >= 16, K % 16 == 0, pointers 16-byte aligned.
+ */
+qlin_status qlin_quantize_act_static(qlin_qtype qtype, int64_t M, int64_t K, const void *x,
+                                     const float *input_scale, void *qx, qlin_stream_t stream);
+
+/*
+ * W8A16 weight-only linear ("Nano-vLLM-MoE" README, FP8 W8A16 Setup: FP8->BF16
+ * dequant GEMM, bf16 x bf16 with fp32 accumulation; "Nano-vLLM-MOE" README,
+ * 关键设计 W8A16 item: INT8 weights dequantized to BF16 for a standard matmul):
+ *   y[m,n] = bf16( w_scale[n] * sum_k x[m,k] * deq(qw[n,k]) + bias[n] )
+ * deq() is exact (every INT8 and E4M3 value is a BF16 value); the per-channel
+ * scale factors out of the k-sum and is applied in fp32 in the epilogue;
+ * accumulation is fp32; the output is rounded to BF16 (nearest even).
+ *   x [M,K] BF16, qw [N,K] codes, w_scale [N] fp32, bias [N] BF16 or NULL,
+ *   y [M,N] BF16 output.  ws/ws_bytes: workspace of
+ *   qlin_workspace_bytes(QLIN_OP_W8A16_LINEAR, ...) bytes (may be NULL when that is 0).
+ * Requirements: M >= 0, K >= 16, N >= 16, K % 16 == 0, N % 16 == 0, pointers
+ * 16-byte aligned, y must not overlap any input.
+ */
+qlin_status qlin_w8a16_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                              const void *qw, const float *w_scale, const void *bias, void *y,
+                              void *ws, size_t ws_bytes, qlin_stream_t stream);
+
+/*
+ * W8A8 static linear ("Nano-vLLM-MOE" README, 关键设计 W8A8 static item;
+ * "Nano-vLLM-MoE" README, FP8 W8A8 static Setup: 8-bit GEMM + custom epilogue):
+ *   qx = quantize_act_static(x, input_scale)           (into the workspace)
+ *   acc[m,n] = sum_k deq(qx[m,k]) * deq(qw[n,k])       (INT8: exact int32;
+ *                                                        E4M3: fp32 accumulate)
+ *   y[m,n] = bf16( acc * (input_scale * w_scale[n]) + bias[n] )
+ * The INT8 accumulator is exact for every input (|acc| <= 127*127*K < 2^31).
+ *   x [M,K] BF16, input_scale fp32 scalar (device), qw [N,K] codes of the same
+ *   qtype, w_scale [N], bias [N] BF16 or NULL, y [M,N] BF16.
+ *   ws: qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N) bytes.
+ * Requirements as for qlin_w8a16_linear.
+ */
+qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                             const float *input_scale, const void *qw, const float *w_scale,
+                             const void *bias, void *y, void *ws, size_t ws_bytes,
+                             qlin_stream_t stream);
+
+/*
+ * Raw INT8 GEMM accumulator, the integer core of the INT8 W8A8 linear, exposed
+ * so it can be checked bit for bit: acc[m,n] = sum_k qx[m,k] * qw[n,k] (int32).
+ *   qx [M,K] int8, qw [N,K] int8, acc [M,N] int32 (device).
+ *   ws: qlin_workspace_bytes(QLIN_OP_I8_GEMM_S32, QLIN_INT8, M, K, N) bytes.
+ * Requirements as for qlin_w8a16_linear.
+ */
+qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, const void *qw,
+                             int32_t *acc, void *ws, size_t ws_bytes, qlin_stream_t stream);
+
+/* Workspace bytes an operation needs for these sizes (0 if none).  Returns
+ * (size_t)-1 for invalid arguments. */
+size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, int64_t N);
+
+/* Synchronizes `stream`, then reports and clears the device status word of the
+ * current device: QLIN_OK, or QLIN_ERR_TIMEOUT if a bounded device-side wait ran
+ * out since the last call, or QLIN_ERR_CUDA if the stream reported an error. */
+qlin_status qlin_get_device_status(qlin_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *qlin_status_string(qlin_status status);
+
+/* Name of the kernel (or kernel sequence, joined by '+') that the given
+ * operation launches for these sizes; "invalid" for arguments it would reject.
+ * Pure host function: no device work. */
+const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, int64_t N);
+
+/* Total number of kernels this process has enqueued through the library so far
+ * (all devices, all streams; memsets not counted).  Host-side counter. */
+uint64_t qlin_launch_count(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int qlin_version(void);
+
+/*
+ * Failure-detection check: launches one thread that waits for *flag to become
+ * non-zero for at most timeout_ns nanoseconds of GPU global time (capped at
+ * 1e9).  If the flag is still zero it sets the device status word to
+ * QLIN_ERR_TIMEOUT and returns; it never hangs.  flag is a device pointer.
+ */
+qlin_status qlin_debug_wait_flag(const uint32_t *flag, uint64_t timeout_ns, qlin_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLIN_H_ */

@@ -1,0 +1,90 @@
+"""Host-side checks of the C ABI (not gpu): the library loads, exports every
+function include/qlin.h declares, and rejects bad arguments before touching a
+device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from bit_quantized_linear_gb300 import build
+    build.build()
+    from bit_quantized_linear_gb300 import capi as c
+    return c
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "qlin.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qlin_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["qlin_quantize_weight", "qlin_quantize_act_static", "qlin_w8a16_linear", "qlin_w8a8_linear",
+              "qlin_act_scale_from_calib", "qlin_i8_gemm_s32", "qlin_workspace_bytes"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(capi):
+    L = ctypes.CDLL(capi.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    assert sorted(capi.EXPORTS) == declared_functions()
+
+
+def test_status_strings_and_version(capi):
+    assert capi.status_string(0) == "QLIN_OK"
+    assert capi.status_string(5) == "QLIN_ERR_TIMEOUT"
+    assert capi.lib().qlin_version() >= 100
+
+
+def test_workspace_sizes(capi):
+    ws = capi.qlin_workspace_bytes
+    assert ws(capi.QLIN_OP_ACT_SCALE, "int8", 32768, 2048, 0) >= 4
+    assert ws(capi.QLIN_OP_W8A8_LINEAR, "e4m3", 1024, 2048, 11008) >= 1024 * 2048
+    assert ws(capi.QLIN_OP_W8A8_LINEAR, "int8", 0, 2048, 11008) == 0
+    assert ws(capi.QLIN_OP_W8A16_LINEAR, 7, 1, 16, 16) == 2 ** 64 - 1
+
+
+def test_invalid_arguments_rejected_on_host(capi):
+    L = capi.lib()
+    P = ctypes.c_void_p
+    good = P(4096)  # never dereferenced: validation fails before any launch
+    odd = P(4096 + 8)
+    INV, WS = capi.QLIN_ERR_INVALID_ARG, capi.QLIN_ERR_WORKSPACE
+    # unknown qtype
+    assert L.qlin_w8a16_linear(9, 1, 64, 64, good, good, good, None, good, None, 0, None) == INV
+    # K, N not multiples of 16 / too small / negative M
+    assert L.qlin_w8a16_linear(0, 1, 72, 64, good, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_linear(0, 1, 64, 40, good, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_linear(0, -1, 64, 64, good, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_linear(0, 1, 0, 64, good, good, good, None, good, None, 0, None) == INV
+    # NULL and misaligned pointers
+    assert L.qlin_w8a16_linear(0, 1, 64, 64, None, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_linear(0, 1, 64, 64, odd, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_linear(0, 1, 64, 64, good, good, good, odd, good, None, 0, None) == INV
+    # W8A8 needs a workspace large enough for the quantized activations
+    assert L.qlin_w8a8_linear(1, 4, 64, 64, good, good, good, good, None, good, None, 0, None) == WS
+    assert L.qlin_w8a8_linear(1, 4, 64, 64, good, good, good, good, None, good, good, 16, None) == WS
+    assert L.qlin_act_scale_from_calib(0, 8, 64, good, good, None, 0, None) == WS
+    assert L.qlin_quantize_weight(0, 4, 24, good, good, good, None) == INV
+    assert L.qlin_quantize_act_static(1, 4, 64, good, None, good, None) == INV
+    assert L.qlin_i8_gemm_s32(4, 64, 64, good, good, None, None, 0, None) == INV
+    assert L.qlin_debug_wait_flag(None, 1000, None) == INV
+
+
+def test_no_device_is_reported_not_crashed(capi):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    L = capi.lib()
+    P = ctypes.c_void_p
+    good = P(4096)
+    st = L.qlin_w8a16_linear(0, 1, 64, 64, good, good, good, None, good, None, 0, None)
+    assert st in (capi.QLIN_ERR_UNSUPPORTED, capi.QLIN_ERR_CUDA)

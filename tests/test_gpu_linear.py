@@ -1,0 +1,243 @@
+"""GPU parity of the linears against the oracle (through the C ABI).
+
+BF16 outputs: within the stated tolerance of the fp64 oracle on the SAME
+quantized operands (so only accumulation and output rounding are measured).
+INT8 accumulator: bit-exact.  Full-size workloads are checked on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_quantized_linear_gb300 import synth
+from _helpers import check_tol, from_dev_bf16, sample_rows, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+QT = {"int8": oracle.INT8, "e4m3": oracle.E4M3}
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from bit_quantized_linear_gb300 import capi as c
+    return c
+
+
+def _operands(lin, rows=None):
+    t = synth.make_inputs(lin)
+    q, s = oracle.quantize_weight(QT[lin.qtype], t["w"])
+    return t, q, s
+
+
+def run_w8a16(capi, qt, x, q, s, b):
+    y = capi.w8a16_linear(qt, to_dev_bf16(x), to_dev(q), to_dev(s), None if b is None else to_dev_bf16(b))
+    torch.cuda.synchronize()
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    return from_dev_bf16(y)
+
+
+def run_w8a8(capi, qt, x, sx, q, s, b):
+    y = capi.w8a8_linear(qt, to_dev_bf16(x), to_dev(np.array([sx], np.float32)), to_dev(q), to_dev(s),
+                         None if b is None else to_dev_bf16(b))
+    torch.cuda.synchronize()
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    return from_dev_bf16(y)
+
+
+# ----------------------------------------------------------------- W8A16
+def w8a16_case(capi, qt, M, K, N, with_bias, seed_tag, rows=None, outliers=False):
+    rng = synth.rng_for("test-w8a16", 0, f"{qt}-{M}x{K}x{N}-{seed_tag}", "all")
+    outl = synth.outlier_channels(K, rng) if outliers else None
+    w = synth.weights(N, K, rng)
+    x = synth.activations(M, K, rng, outl)
+    b = synth.bias(N, rng) if with_bias else None
+    q, s = oracle.quantize_weight(QT[qt], w)
+    y = run_w8a16(capi, qt, x, q, s, b)
+    if rows is None:
+        ref = oracle.w8a16(QT[qt], x, q, s, b)
+        return check_tol(y, ref, f"w8a16 {qt} {M}x{K}x{N}")
+    ref = oracle.w8a16(QT[qt], x, q, s, b, rows=rows)
+    return check_tol(y[rows], ref, f"w8a16 {qt} {M}x{K}x{N} rows")
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 17, 31, 64, 127, 129, 255, 256, 257])
+def test_w8a16_ragged_m(capi, qt, M):
+    w8a16_case(capi, qt, M, 384, 272, True, "ragged-m")
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+@pytest.mark.parametrize("M,K,N", [(1, 16, 16), (5, 48, 16), (33, 80, 144), (300, 1040, 400), (1024, 512, 384)])
+def test_w8a16_ragged_kn(capi, qt, M, K, N):
+    w8a16_case(capi, qt, M, K, N, M % 2 == 1, "ragged-kn", outliers=True)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_w8a16_int8_small_workload(capi, M):
+    """INT8 W8A16 single linear K=N=1024, M in {1,16}, full output checked."""
+    lin = [l for l in synth.workload(synth.SMALL).linears if l.M == M][0]
+    t, q, s = _operands(lin)
+    y = run_w8a16(capi, "int8", t["x"], q, s, None)
+    check_tol(y, oracle.w8a16(oracle.INT8, t["x"], q, s), f"small M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 128, 256])
+@pytest.mark.parametrize("name", ["q_proj", "gate_up_proj", "down_proj"])
+def test_w8a16_decode7b_full_size(capi, name, M):
+    """FP8-E4M3 W8A16 decode sweep at full size, sampled output rows."""
+    lin = [l for l in synth.workload(synth.DECODE7B).linears if l.name == name and l.M == M][0]
+    t, q, s = _operands(lin)
+    y = run_w8a16(capi, "e4m3", t["x"], q, s, None)
+    rows = sample_rows(M, 8)
+    check_tol(y[rows], oracle.w8a16(oracle.E4M3, t["x"], q, s, rows=rows), f"{name} M={M}")
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+def test_w8a16_zero_weight_gives_bias(capi, qt):
+    M, K, N = 5, 64, 48
+    rng = np.random.default_rng(0)
+    b = synth.bias(N, rng)
+    x = synth.activations(M, K, rng)
+    q, s = oracle.quantize_weight(QT[qt], np.zeros((N, K), np.float32))
+    y = run_w8a16(capi, qt, x, q, s, b)
+    assert np.array_equal(y, np.broadcast_to(b, (M, N)))
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+def test_w8a16_power_of_two_scaling_bitexact(capi, qt):
+    """W * 2^j: same codes, scales * 2^j, so the BF16 output scales bit-exactly."""
+    M, K, N = 9, 256, 128
+    rng = np.random.default_rng(3)
+    w = synth.weights(N, K, rng)
+    x = synth.activations(M, K, rng)
+    q1, s1 = oracle.quantize_weight(QT[qt], w)
+    q2, s2 = oracle.quantize_weight(QT[qt], w * np.float32(16))
+    assert np.array_equal(q1, q2)
+    y1 = synth.bf16_bits_to_f32(run_w8a16(capi, qt, x, q1, s1, None))
+    y2 = synth.bf16_bits_to_f32(run_w8a16(capi, qt, x, q2, s2, None))
+    assert np.array_equal(y2, y1 * np.float32(16))
+
+
+def test_w8a16_m0_is_noop(capi):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    qw = torch.zeros((32, 64), dtype=torch.uint8, device="cuda")
+    s = torch.ones(32, device="cuda")
+    y = capi.w8a16_linear("int8", x, qw, s)
+    assert y.shape == (0, 32)
+
+
+# ------------------------------------------------------------------ W8A8
+def w8a8_case(capi, qt, M, K, N, with_bias, tag, rows=None, outliers=False):
+    rng = synth.rng_for("test-w8a8", 0, f"{qt}-{M}x{K}x{N}-{tag}", "all")
+    outl = synth.outlier_channels(K, rng) if outliers else None
+    w = synth.weights(N, K, rng)
+    cal = synth.activations(1024, K, rng, outl)
+    x = synth.activations(M, K, rng, outl)
+    b = synth.bias(N, rng) if with_bias else None
+    q, s = oracle.quantize_weight(QT[qt], w)
+    sx = oracle.act_scale(QT[qt], cal)
+    y = run_w8a8(capi, qt, x, sx, q, s, b)
+    qx = oracle.quantize_act(QT[qt], x, sx)
+    ref = oracle.w8a8(QT[qt], qx, sx, q, s, b, rows=rows)
+    return check_tol(y if rows is None else y[rows], ref, f"w8a8 {qt} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+@pytest.mark.parametrize("M", [1, 3, 16, 127, 129, 256, 257, 1024])
+def test_w8a8_ragged_m(capi, qt, M):
+    w8a8_case(capi, qt, M, 512, 272, True, "ragged-m", outliers=True)
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+@pytest.mark.parametrize("M,K,N", [(1, 16, 16), (7, 48, 32), (130, 1040, 400), (2048, 2048, 512)])
+def test_w8a8_ragged_kn(capi, qt, M, K, N):
+    w8a8_case(capi, qt, M, K, N, M % 2 == 0, "ragged-kn")
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3])
+def test_w8a8_int8_3b_workload(capi, idx):
+    """INT8 W8A8 static on the 3B microbench shapes with bias, full size, full output."""
+    lin = synth.workload(synth.W8A8_3B).linears[idx]
+    t, q, s = _operands(lin)
+    sx = oracle.act_scale(oracle.INT8, t["cal"])
+    y = run_w8a8(capi, "int8", t["x"], sx, q, s, t["bias"])
+    rows = None if lin.M <= 256 else sample_rows(lin.M, 32)
+    qx = oracle.quantize_act(oracle.INT8, t["x"], sx)
+    ref = oracle.w8a8(oracle.INT8, qx, sx, q, s, t["bias"], rows=rows)
+    check_tol(y if rows is None else y[rows], ref, f"3b {lin.name} M={lin.M}")
+
+
+@pytest.mark.parametrize("M", [1024, 4096])
+@pytest.mark.parametrize("K,N", [(2048, 11008), (11008, 2048), (2048, 2048)])
+def test_w8a8_e4m3_prefill(capi, M, K, N):
+    """FP8-E4M3 W8A8 static prefill shapes (M up to 4096 here; the largest M are
+    in the slow set), sampled output rows."""
+    lin = [l for l in synth.workload(synth.PREFILL).linears if l.M == M and l.K == K and l.N == N][0]
+    t, q, s = _operands(lin)
+    sx = oracle.act_scale(oracle.E4M3, t["cal"])
+    y = run_w8a8(capi, "e4m3", t["x"], sx, q, s, None)
+    rows = sample_rows(M, 16)
+    qx = oracle.quantize_act(oracle.E4M3, t["x"][rows], sx)
+    ref = oracle.w8a8(oracle.E4M3, qx, sx, q, s)
+    check_tol(y[rows], ref, f"prefill {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+def test_w8a8_zero_weight_gives_bias(capi, qt):
+    M, K, N = 6, 64, 32
+    rng = np.random.default_rng(4)
+    b = synth.bias(N, rng)
+    x = synth.activations(M, K, rng)
+    q, s = oracle.quantize_weight(QT[qt], np.zeros((N, K), np.float32))
+    y = run_w8a8(capi, qt, x, np.float32(0.05), q, s, b)
+    assert np.array_equal(y, np.broadcast_to(b, (M, N)))
+
+
+# ----------------------------------------------------- INT8 accumulator
+@pytest.mark.parametrize("M,K,N", [(1, 16, 16), (3, 48, 32), (127, 1040, 144), (256, 11008, 2048),
+                                   (1024, 2048, 1024)])
+def test_i8_gemm_bitexact(capi, M, K, N):
+    rng = np.random.default_rng(M * 7 + K)
+    qx = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    acc = capi.i8_gemm_s32(to_dev(qx.view(np.uint8)), to_dev(qw.view(np.uint8))).cpu().numpy()
+    assert np.array_equal(acc, oracle.i8_gemm(qx, qw))
+
+
+def test_i8_gemm_worst_case_magnitude(capi):
+    """All +-127 at K=18944: |acc| = 127*127*18944, the largest the layer meets."""
+    K = 18944
+    qx = np.full((130, K), 127, np.int8)
+    qx[1::2] = -127
+    qw = np.full((144, K), 127, np.int8)
+    qw[::3] = -127
+    acc = capi.i8_gemm_s32(to_dev(qx.view(np.uint8)), to_dev(qw.view(np.uint8))).cpu().numpy()
+    ref = oracle.i8_gemm(qx, qw)
+    assert np.abs(ref).max() == 127 * 127 * K
+    assert np.array_equal(acc, ref)
+
+
+def test_i8_gemm_one_hot(capi):
+    rng = np.random.default_rng(12)
+    M, K, N = 40, 256, 64
+    qx = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    perm = rng.permutation(K)[:N]
+    qw = np.zeros((N, K), np.int8)
+    qw[np.arange(N), perm] = 127
+    acc = capi.i8_gemm_s32(to_dev(qx.view(np.uint8)), to_dev(qw.view(np.uint8))).cpu().numpy()
+    assert np.array_equal(acc, 127 * qx[:, perm].astype(np.int32))
+
+
+# ------------------------------------------------------ failure detection
+def test_bounded_wait_reports_timeout(capi):
+    flag = torch.zeros(4, dtype=torch.int32, device="cuda")
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    capi.qlin_debug_wait_flag(flag, 2_000_000)  # nothing sets the flag: gives up after 2 ms
+    assert capi.qlin_get_device_status() == capi.QLIN_ERR_TIMEOUT
+    assert capi.qlin_get_device_status() == capi.QLIN_OK  # cleared by the read
+    flag.fill_(1)
+    capi.qlin_debug_wait_flag(flag, 2_000_000)
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    y = capi.w8a16_linear("int8", torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda"),
+                          torch.zeros((16, 64), dtype=torch.uint8, device="cuda"), torch.ones(16, device="cuda"))
+    torch.cuda.synchronize()  # the context is still usable
+    assert y.float().abs().sum().item() == 0.0
