@@ -43,6 +43,12 @@ struct GemmArgs {
 
 cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 
+// tcgen05 kernels (gemm_tc.cu)
+cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
+cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
+int w8_swap_bnt(int64_t M);
+int w8_swap_splits(int64_t M, int64_t K, int64_t N, int sms);
+
 cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
                               cudaStream_t st);
 

@@ -71,13 +71,23 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_QUANTIZE_WEIGHT: return "k_quantize_weight";
     case QLIN_OP_ACT_SCALE: return "k_absmax_bf16+k_scale_finalize";
     case QLIN_OP_QUANTIZE_ACT: return "k_quantize_act";
-    case QLIN_OP_W8A16_LINEAR:
+    case QLIN_OP_W8A16_LINEAR: {
+      if (check_linear_shape(M, K, N)) return "invalid";
+      if (M == 0) return "none";
+      static const char *names[5] = {"k_w8_swap<16>", "k_w8_swap<32>", "k_w8_swap<64>", "k_w8_swap<128>",
+                                     "k_w8_swap<256>"};
+      const int b = w8_swap_bnt(M);
+      return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : b == 128 ? 3 : 4];
+    }
     case QLIN_OP_I8_GEMM_S32:
       if (check_linear_shape(M, K, N)) return "invalid";
       return M == 0 ? "none" : "k_gemm_simt";
     case QLIN_OP_W8A8_LINEAR:
       if (check_linear_shape(M, K, N)) return "invalid";
-      return M == 0 ? "none" : "k_quantize_act+k_gemm_simt";
+      if (M == 0) return "none";
+      if (qtype == QLIN_E4M3) return (N % 256 == 0 || N > 1024) ? "k_quantize_act+k_fp8_gemm<256>"
+                                                                  : "k_quantize_act+k_fp8_gemm<128>";
+      return "k_quantize_act+k_gemm_simt";
   }
   return "invalid";
 }
@@ -135,8 +145,8 @@ qlin_status qlin_quantize_act_static(qlin_qtype qtype, int64_t M, int64_t K, con
                                      const float *input_scale, void *qx, qlin_stream_t stream) {
   if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
   if (M < 0 || K < 16 || (K % 16)) return QLIN_ERR_INVALID_ARG;
-  if (!x || !input_scale || !qx || !al16(x) || !al16(qx) || ((uintptr_t)input_scale & 3u))
-    return QLIN_ERR_INVALID_ARG;
+  if (!input_scale || ((uintptr_t)input_scale & 3u)) return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !qx || !al16(x) || !al16(qx))) return QLIN_ERR_INVALID_ARG;
   DeviceInfo *dev;
   if (qlin_status s = current_device(&dev)) return s;
   if (M == 0) return QLIN_OK;
@@ -148,16 +158,15 @@ qlin_status qlin_w8a16_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N,
                               void *ws, size_t ws_bytes, qlin_stream_t stream) {
   if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
   if (qlin_status s = check_linear_shape(M, K, N)) return s;
-  if (!x || !qw || !w_scale || !y || !al16(x) || !al16(qw) || !al16(w_scale) || !al16(y) ||
-      (bias && !al16(bias)))
-    return QLIN_ERR_INVALID_ARG;
+  if (!qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias))) return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
   const size_t need = qlin_workspace_bytes(QLIN_OP_W8A16_LINEAR, qtype, M, K, N);
   if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
   DeviceInfo *dev;
   if (qlin_status s = current_device(&dev)) return s;
   if (M == 0) return QLIN_OK;
   GemmArgs g{kW8A16, qtype, M, K, N, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
-  return from_cuda(launch_gemm_simt(g, *dev, (cudaStream_t)stream));
+  return from_cuda(launch_w8a16_swap(g, *dev, (cudaStream_t)stream));
 }
 
 qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
@@ -166,9 +175,10 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
                              qlin_stream_t stream) {
   if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
   if (qlin_status s = check_linear_shape(M, K, N)) return s;
-  if (!x || !input_scale || !qw || !w_scale || !y || !al16(x) || !al16(qw) || !al16(w_scale) ||
-      !al16(y) || (bias && !al16(bias)) || ((uintptr_t)input_scale & 3u))
+  if (!input_scale || !qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias)) ||
+      ((uintptr_t)input_scale & 3u))
     return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
   const size_t need = qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N);
   if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
   DeviceInfo *dev;
@@ -177,13 +187,15 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaError_t e = launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st)) return QLIN_ERR_CUDA;
   GemmArgs g{kW8A8, qtype, M, K, N, ws, qw, w_scale, input_scale, (const uint16_t *)bias, y};
+  if (qtype == QLIN_E4M3) return from_cuda(launch_fp8_gemm(g, *dev, st));
   return from_cuda(launch_gemm_simt(g, *dev, st));
 }
 
 qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, const void *qw,
                              int32_t *acc, void *ws, size_t ws_bytes, qlin_stream_t stream) {
   if (qlin_status s = check_linear_shape(M, K, N)) return s;
-  if (!qx || !qw || !acc || !al16(qx) || !al16(qw) || !al16(acc)) return QLIN_ERR_INVALID_ARG;
+  if (!qw || !al16(qw)) return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!qx || !acc || !al16(qx) || !al16(acc))) return QLIN_ERR_INVALID_ARG;
   const size_t need = qlin_workspace_bytes(QLIN_OP_I8_GEMM_S32, QLIN_INT8, M, K, N);
   if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
   DeviceInfo *dev;

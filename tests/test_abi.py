@@ -76,6 +76,7 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert L.qlin_quantize_weight(0, 4, 24, good, good, good, None) == INV
     assert L.qlin_quantize_act_static(1, 4, 64, good, None, good, None) == INV
     assert L.qlin_i8_gemm_s32(4, 64, 64, good, good, None, None, 0, None) == INV
+    assert L.qlin_i8_gemm_s32(4, 64, 64, good, None, good, None, 0, None) == INV
     assert L.qlin_debug_wait_flag(None, 1000, None) == INV
 
 
