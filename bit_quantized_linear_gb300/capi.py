@@ -27,7 +27,10 @@ QTYPES = {"int8": QLIN_INT8, "e4m3": QLIN_E4M3}
 EXPORTS = ["qlin_quantize_weight", "qlin_act_scale_from_calib", "qlin_quantize_act_static",
            "qlin_w8a16_linear", "qlin_w8a8_linear", "qlin_i8_gemm_s32", "qlin_workspace_bytes",
            "qlin_get_device_status", "qlin_status_string", "qlin_version", "qlin_debug_wait_flag",
-           "qlin_kernel_name", "qlin_launch_count"]
+           "qlin_kernel_name", "qlin_launch_count", "qlin_w8a8_linear_noalloc"]
+
+# Size of the library-owned scratch of qlin_w8a8_linear_noalloc (QLIN_W8A8_NOALLOC_SCRATCH_BYTES).
+W8A8_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class QlinError(RuntimeError):
@@ -55,6 +58,7 @@ def _load() -> ctypes.CDLL:
         "qlin_debug_wait_flag": [P, ctypes.c_uint64, P],
         "qlin_kernel_name": [I, I, I64, I64, I64],
         "qlin_launch_count": [],
+        "qlin_w8a8_linear_noalloc": [I, I64, I64, I64, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -138,6 +142,15 @@ def qlin_w8a8_linear(qtype, x, input_scale, qw, w_scale, bias, y, ws, stream=Non
     wp, wb = _ws(ws)
     _check(_lib.qlin_w8a8_linear(_qt(qtype), M, K, N, _p(x), _p(input_scale), _p(qw), _p(w_scale),
                                  _p(bias), _p(y), wp, wb, _stream(stream)), "qlin_w8a8_linear")
+
+
+def qlin_w8a8_linear_noalloc(qtype, x, input_scale, qw, w_scale, bias, y, stream=None):
+    """W8A8 static linear without a workspace (see qlin_w8a8_linear_noalloc in
+    include/qlin.h): for callers that cannot allocate device memory."""
+    M, K = x.shape
+    N = qw.shape[0]
+    _check(_lib.qlin_w8a8_linear_noalloc(_qt(qtype), M, K, N, _p(x), _p(input_scale), _p(qw), _p(w_scale),
+                                         _p(bias), _p(y), _stream(stream)), "qlin_w8a8_linear_noalloc")
 
 
 def qlin_i8_gemm_s32(qx, qw, acc, ws=None, stream=None):

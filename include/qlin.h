@@ -168,6 +168,34 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
 qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, const void *qw,
                              int32_t *acc, void *ws, size_t ws_bytes, qlin_stream_t stream);
 
+/*
+ * W8A8 static linear for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that run where cudaMalloc (and any allocating library, torch included) is not
+ * available or not allowed: inference plugins handed a fixed memory budget,
+ * code enqueued while a stream is being captured into a CUDA graph, or
+ * runtimes that must not grow device memory after start-up.  It computes
+ * exactly what qlin_w8a8_linear computes, with the same arguments minus the
+ * workspace: the quantized activations go to a scratch array that the library
+ * holds in device memory of its own (a file-scope __device__ array of
+ * QLIN_W8A8_NOALLOC_SCRATCH_BYTES bytes, 32 MiB, which every GPU that loads the
+ * library keeps until the process exits).
+ *   - Sizes whose workspace (qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype,
+ *     M, K, N)) exceeds QLIN_W8A8_NOALLOC_SCRATCH_BYTES are rejected with
+ *     QLIN_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (once per device, with that device current); make that first call before
+ *     any stream capture begins.
+ *   - Every call on a device shares the one scratch array, and each call
+ *     overwrites what the previous call left there.  Calls that can overlap on
+ *     the GPU (different streams without ordering) race on it; order them.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define QLIN_W8A8_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+qlin_status qlin_w8a8_linear_noalloc(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                                     const float *input_scale, const void *qw, const float *w_scale,
+                                     const void *bias, void *y, qlin_stream_t stream);
+
 /* Workspace bytes an operation needs for these sizes (0 if none).  Returns
  * (size_t)-1 for invalid arguments. */
 size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, int64_t N);
