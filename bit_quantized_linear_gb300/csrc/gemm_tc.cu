@@ -198,35 +198,64 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 1) tmem_dealloc(tmem, BN);
 }
 
-// ===================================================== W8A16 swap-AB GEMM
+// ========================================== swap-AB GEMM with A in tensor memory
+// Output channels on the 128 TMEM lanes, tokens on the MMA N dimension (16..256).
+// The 8-bit weight codes stream through a deep shared-memory ring; converter
+// warps turn each 128 x 64 tile into exact BF16 and store it straight into a
+// ring of A operands in tensor memory (tcgen05.st), so the converted weights
+// never touch shared memory; the MMA reads A from TMEM and the activations (B)
+// from a 128-byte-swizzled shared-memory ring.
+//
+// Modes:  W8A16: B = BF16 activations, fp32 accumulation over all of K,
+//                epilogue y = acc * s_w[n] + bias[n].
+//         I8:    B = activation codes stored as integer-valued BF16; the MMA
+//                accumulates fp32 over chunks of 512 k, where every partial sum
+//                is an integer below 127*127*512 < 2^23 and therefore exact; the
+//                epilogue warps add each chunk into int32 registers, so the full
+//                accumulator is the exact integer sum.  Output: raw int32, or
+//                y = acc * (s_x * s_w[n]) + bias[n].
+enum SwapMode { kSwapW8A16 = 0, kSwapI8Scaled = 1, kSwapI8Raw = 2 };
+
 struct SwapParams {
   int M, N, K;
   int splits;  // CTAs per cluster along K (gridDim.z)
+  int units;   // output tiles: n-tiles x token tiles
+  int ntiles;  // n-tiles (128 channels each)
   const float *w_scale;
+  const float *x_scale;
   const uint16_t *bias;
-  uint16_t *y;
+  void *y;
   unsigned *status;
 };
 
 template <int BNT>
-struct SwapCfg {
+struct DqCfg {
   static constexpr int BM = 128, BK = 64;
-  static constexpr int CONV_BYTES = BM * BK * 2;  // BF16 A tile, 128-byte swizzle
-  static constexpr int X_BYTES = BNT * BK * 2;    // BF16 B tile, 128-byte swizzle
-  static constexpr int RAW_BYTES = BM * BK;       // 8-bit weight tile, row-major 64 B rows
-  static constexpr int STAGE_BYTES = CONV_BYTES + X_BYTES + RAW_BYTES;
-  static constexpr int STAGES = (180 * 1024) / STAGE_BYTES > 8 ? 8 : (180 * 1024) / STAGE_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
-  static constexpr int TMEM_COLS = BNT < 32 ? 32 : BNT;
+  static constexpr int RAW_BYTES = BM * BK;     // 8-bit weight tile, 64-byte swizzle
+  static constexpr int X_BYTES = BNT * BK * 2;  // BF16 activation tile, 128-byte swizzle
+  static constexpr int X = BNT <= 64 ? (65536 / X_BYTES > 16 ? 16 : 65536 / X_BYTES) : (BNT == 128 ? 6 : 3);
+  static constexpr int RING = 200 * 1024;
+  static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
+  static constexpr int R = R0 > 16 ? 16 : R0;
+  static constexpr int X_OFF = 0, RAW_OFF = X * X_BYTES, BAR_OFF = RAW_OFF + R * RAW_BYTES;
+  static constexpr int SMEM = BAR_OFF + 1024 + 1024;  // alignment slack + barriers
+  static constexpr int ND = BNT <= 128 ? 2 : 1;        // accumulator buffers in TMEM
+  static constexpr int DSTRIDE = BNT <= 64 ? 64 : BNT;
+  static constexpr int ACOL = BNT <= 64 ? 128 : 256;   // first TMEM column of the A ring
+  static constexpr int NA = BNT <= 64 ? 12 : 8;        // A stages, 32 columns (64 BF16 k) each
+  static constexpr int QUADS = 3;                      // converter warp quads
+  static constexpr int THREADS = 640;                  // 20 warps
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
-  static_assert(BM * BNT * 4 <= STAGES * STAGE_BYTES, "split-K partial tile must fit the stage ring");
+  static_assert(ACOL + NA * 32 <= 512, "TMEM columns");
+  static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(2 * (R + X + NA + ND) * 8 + 16 <= 1024, "barrier area");
 };
 
-// 16 weight codes -> 16 exact BF16 values (two 16-byte chunks, k order kept).
+// 16 weight codes -> 16 exact BF16 values packed in 8 words (k order kept).
 template <int QT>
-__device__ __forceinline__ void convert16(uint4 raw, uint4 &lo, uint4 &hi) {
-  uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t o[8];
+__device__ __forceinline__ void convert16(uint4 raw, uint32_t *o) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   if constexpr (QT == QLIN_INT8) {
     // byte b (two's complement) -> fp32 via the 2^23 + (b ^ 0x80) bit pattern, minus 2^23 + 128: exact.
 #pragma unroll
@@ -254,189 +283,302 @@ __device__ __forceinline__ void convert16(uint4 raw, uint4 &lo, uint4 &hi) {
       }
     }
   }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-template <int BNT, int QT>
-__global__ void __launch_bounds__(256, 1)
-    k_w8_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, SwapParams p) {
-  using C = SwapCfg<BNT>;
+// Writes 4 consecutive output channels of one token row (S > 1 path).
+template <int MODE>
+__device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const uint32_t (&v)[4]) {
+  if constexpr (MODE == kSwapI8Raw) {
+    *reinterpret_cast<uint4 *>((int32_t *)p.y + (size_t)m * p.N + n) = make_uint4(v[0], v[1], v[2], v[3]);
+  } else {
+    const float sx = MODE == kSwapI8Scaled ? __ldg(p.x_scale) : 1.0f;
+    uint32_t o[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float a[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int k = 2 * h + e;
+        const float acc = MODE == kSwapW8A16 ? __uint_as_float(v[k]) : (float)(int)v[k];
+        a[e] = acc * (sx * __ldg(p.w_scale + n + k));
+        if (p.bias) a[e] += bf16_bits_to_f32(__ldg(p.bias + n + k));
+      }
+      o[h] = pack_bf16x2(a[0], a[1]);
+    }
+    *reinterpret_cast<uint2 *>((uint16_t *)p.y + (size_t)m * p.N + n) = make_uint2(o[0], o[1]);
+  }
+}
+
+template <int BNT, int QT, int MODE>
+__global__ void __launch_bounds__(640, 1)
+    k_w8_dq(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, SwapParams p) {
+  using C = DqCfg<BNT>;
+  constexpr bool kI8 = MODE != kSwapW8A16;
+  constexpr int CH = kI8 ? 8 : (1 << 30);  // k-blocks per exactly accumulated chunk
+  static_assert(!kI8 || BNT <= 64, "int32 sums live in registers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint64_t *full = (uint64_t *)(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t *conv_full = full + C::STAGES;
-  uint64_t *empty = conv_full + C::STAGES;
-  uint64_t *acc_full = empty + C::STAGES;
-  uint32_t *tmem_slot = (uint32_t *)(acc_full + 1);
+  uint8_t *xs = smem + C::X_OFF, *raws = smem + C::RAW_OFF;
+  uint64_t *bars = (uint64_t *)(smem + C::BAR_OFF);
+  uint64_t *raw_full = bars, *raw_empty = raw_full + C::R;
+  uint64_t *x_full = raw_empty + C::R, *x_empty = x_full + C::X;
+  uint64_t *a_full = x_empty + C::X, *a_empty = a_full + C::NA;
+  uint64_t *acc_full = a_empty + C::NA, *acc_empty = acc_full + C::ND;
+  uint32_t *tmem_slot = (uint32_t *)(acc_empty + C::ND);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * C::BM, m0 = blockIdx.y * BNT;
   const int split = blockIdx.z, S = p.splits;
   const int KB = (p.K + C::BK - 1) / C::BK;
   const int kb0 = (int)((int64_t)split * KB / S), kb1 = (int)((int64_t)(split + 1) * KB / S);
   const int nkb = kb1 - kb0;
+  const int G = gridDim.x;
+  const int my_units = (p.units - (int)blockIdx.x + G - 1) / G;
+  const int total = my_units * nkb;
+  const int chunks_per_unit = (nkb + CH - 1) / CH;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&conv_full[s], 4);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < C::R; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);  // the four warps of the quad that read the tile
     }
-    mbar_init(acc_full, 1);
+    for (int s = 0; s < C::X; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], 1);
+    }
+    for (int s = 0; s < C::NA; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < C::ND; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 4);  // the epilogue quad
+    }
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {  // ---------------- TMA producer
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % C::STAGES;
-      if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
-        *abort_flag = 1;
-        break;
+  if (warp == 0) {  // ------------------------ weight-tile producer
+    if (lane == 0) {
+      for (int i = 0; i < total; ++i) {
+        const int j = i / nkb, kb = i - j * nkb, s = i % C::R;
+        if (i >= C::R && !mbar_wait(&raw_empty[s], ((i / C::R) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int u = blockIdx.x + j * G;
+        mbar_arrive_expect_tx(&raw_full[s], C::RAW_BYTES);
+        tma_load_2d(&tm_w, &raw_full[s], raws + s * C::RAW_BYTES, (kb0 + kb) * C::BK, (u % p.ntiles) * C::BM);
       }
-      uint8_t *st = smem + s * C::STAGE_BYTES;
-      const int kx = (kb0 + i) * C::BK;
-      mbar_arrive_expect_tx(&full[s], C::RAW_BYTES + C::X_BYTES);
-      tma_load_2d(&tm_w, &full[s], st + C::CONV_BYTES + C::X_BYTES, kx, n0);
-      tma_load_2d(&tm_x, &full[s], st + C::CONV_BYTES, kx, m0);
     }
-  } else if (warp == 1 && lane == 0) {  // ---------- MMA issuer
+  } else if (warp == 2) {  // ----------------- activation-tile producer
+    if (lane == 0) {
+      for (int i = 0; i < total; ++i) {
+        const int j = i / nkb, kb = i - j * nkb, s = i % C::X;
+        if (i >= C::X && !mbar_wait(&x_empty[s], ((i / C::X) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        const int u = blockIdx.x + j * G;
+        mbar_arrive_expect_tx(&x_full[s], C::X_BYTES);
+        tma_load_2d(&tm_x, &x_full[s], xs + s * C::X_BYTES, (kb0 + kb) * C::BK, (u / p.ntiles) * BNT);
+      }
+    }
+  } else if (warp == 1) {  // ----------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int cidx = 0;
+      for (int i = 0; i < total && ok; ++i) {
+        const int kb = i % nkb;
+        const bool cstart = (kb % CH) == 0;
+        const bool cend = (kb % CH) == CH - 1 || kb == nkb - 1;
+        const int db = cidx % C::ND;
+        if (cstart && cidx >= C::ND) {
+          if (!mbar_wait(&acc_empty[db], ((cidx / C::ND) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
+        const int sx = i % C::X, sa = i % C::NA;
+        if (!mbar_wait(&x_full[sx], (i / C::X) & 1, abort_flag) || !mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem + db * C::DSTRIDE, at = tmem + C::ACOL + sa * 32;
+        const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::X_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk)  // K = 16 per instruction: 8 TMEM columns of A, 32 bytes of B
+          mma_bf16_ts(dt, at + 8 * kk, bd + 2 * kk, C::IDESC, (!cstart || kk > 0) ? 1u : 0u);
+        mma_commit(&x_empty[sx]);
+        mma_commit(&a_empty[sa]);
+        if (cend) {
+          mma_commit(&acc_full[db]);
+          ++cidx;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp >= 4 && warp < 16) {  // ----- converter quads
+    const int quad = (warp - 4) >> 2, q4 = warp & 3, row = q4 * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % C::STAGES;
-      const uint32_t ph = (i / C::STAGES) & 1;
-      if (!mbar_wait(&full[s], ph, abort_flag) || !mbar_wait(&conv_full[s], ph, abort_flag)) {
+    for (int i = quad; i < total; i += C::QUADS) {
+      const int r = i % C::R, sa = i % C::NA;
+      if (!mbar_wait(&raw_full[r], (i / C::R) & 1, abort_flag)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t a = smem_u32(smem + s * C::STAGE_BYTES);
-      const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(a + C::CONV_BYTES);
+      // row `row` of the raw tile: four 16-byte chunks, 64-byte swizzle (chunk ^ ((row >> 1) & 3))
+      const uint32_t rb = smem_u32(raws + r * C::RAW_BYTES) + row * 64;
+      const int sw = (row >> 1) & 3;
+      uint4 raw[4];
 #pragma unroll
-      for (int kk = 0; kk < C::BK / 16; ++kk)  // K = 16 per instruction (32 bytes)
-        mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC, (i | kk) != 0);
-      mma_commit(&empty[s]);
-    }
-    if (!ok) *abort_flag = 1;
-    mma_commit(acc_full);
-  } else if (warp >= 4) {  // -------------- converters, then epilogue
-    const int ct = threadIdx.x - 128;  // 0..127
-    bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % C::STAGES;
-      if (!mbar_wait(&full[s], (i / C::STAGES) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
-      const uint32_t raw = st + C::CONV_BYTES + C::X_BYTES;
+      for (int c = 0; c < 4; ++c) raw[c] = lds128(rb + ((c ^ sw) << 4));
+      uint32_t words[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = ct + 128 * j;  // 16-byte chunk of the raw tile: row r, quarter qq
-        const int r = c >> 2, qq = c & 3;
-        uint4 lo, hi;
-        convert16<QT>(lds128(raw + r * 64 + qq * 16), lo, hi);
-        const uint32_t row = st + r * 128;
-        sts128(row + (((2 * qq) ^ (r & 7)) << 4), lo);
-        sts128(row + (((2 * qq + 1) ^ (r & 7)) << 4), hi);
-      }
-      fence_proxy_async_smem();
+      for (int c = 0; c < 4; ++c) convert16<QT>(raw[c], words + 8 * c);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&conv_full[s]);
+      if (lane == 0) mbar_arrive(&raw_empty[r]);
+      if (i >= C::NA && !mbar_wait(&a_empty[sa], ((i / C::NA) & 1) ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tmem_st32(tmem + lane_base + C::ACOL + sa * 32, words);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[sa]);
     }
     if (!ok) *abort_flag = 1;
-    // ---- epilogue: lane = output channel n, columns = tokens
-    const int q = warp & 3;
-    const int nl = q * 32 + lane;
-    const int n = n0 + nl;
-    ok = mbar_wait(acc_full, 0, abort_flag) && ok;
-    tc_fence_after();
-    // tcgen05.ld is warp-collective: every lane of the warp takes the same path
-    const bool run = __all_sync(0xffffffffu, ok && !*abort_flag);
-    if (S == 1) {
+  } else if (warp >= 16) {  // ------------------ epilogue quad
+    const int q4 = warp & 3, nl = q4 * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    int cidx = 0;
+    bool ok = true;
+    for (int j = 0; j < my_units && ok; ++j) {
+      const int u = blockIdx.x + j * G;
+      const int n0 = (u % p.ntiles) * C::BM, m0 = (u / p.ntiles) * BNT;
+      const int n = n0 + nl;
       const bool valid = n < p.N;
-      const float sw = valid ? __ldg(p.w_scale + n) : 0.0f;
-      const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
-      if (run) {
-#pragma unroll 1
-        for (int c = 0; c < BNT; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, r);
-          tmem_ld_wait();
-          if (valid) {
+      int32_t sums[kI8 ? BNT : 1];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int m = m0 + c + j;
-              if (m < p.M) p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(fmaf(__uint_as_float(r[j]), sw, b));
+      for (int c = 0; c < (kI8 ? BNT : 1); ++c) sums[c] = 0;
+      for (int ch = 0; ch < chunks_per_unit; ++ch, ++cidx) {
+        const int db = cidx % C::ND;
+        ok = mbar_wait(&acc_full[db], (cidx / C::ND) & 1, abort_flag);
+        tc_fence_after();
+        // tcgen05.ld is warp-collective: every lane of the warp takes the same path
+        const bool run = __all_sync(0xffffffffu, ok && !*abort_flag);
+        if (!run) {
+          ok = false;
+          break;
+        }
+        const uint32_t dt = tmem + lane_base + db * C::DSTRIDE;
+        if constexpr (kI8) {
+#pragma unroll
+          for (int c = 0; c < BNT; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(dt + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sums[c + e] += __float2int_rn(__uint_as_float(r[e]));
+          }
+        } else if (S == 1) {
+          const float sw = valid ? __ldg(p.w_scale + n) : 0.0f;
+          const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
+          uint16_t *y = (uint16_t *)p.y;
+#pragma unroll 1
+          for (int c = 0; c < BNT; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(dt + c, r);
+            tmem_ld_wait();
+            if (valid) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int m = m0 + c + e;
+                if (m < p.M) y[(size_t)m * p.N + n] = f32_to_bf16_bits(fmaf(__uint_as_float(r[e]), sw, b));
+              }
             }
+          }
+        } else {
+          uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // partial tile, [token][channel]
+#pragma unroll 1
+          for (int c = 0; c < BNT; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(dt + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) red[(c + e) * C::BM + nl] = r[e];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[db]);
+      }
+      if constexpr (kI8) {
+        if (ok) {
+          if (S == 1) {
+            if (valid) {
+              if constexpr (MODE == kSwapI8Raw) {
+#pragma unroll
+                for (int c = 0; c < BNT; ++c)
+                  if (m0 + c < p.M) ((int32_t *)p.y)[(size_t)(m0 + c) * p.N + n] = sums[c];
+              } else {
+                const float sc = __ldg(p.x_scale) * __ldg(p.w_scale + n);
+                const float b = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
+#pragma unroll
+                for (int c = 0; c < BNT; ++c)
+                  if (m0 + c < p.M)
+                    ((uint16_t *)p.y)[(size_t)(m0 + c) * p.N + n] = f32_to_bf16_bits(fmaf((float)sums[c], sc, b));
+              }
+            }
+          } else {
+            int32_t *red = reinterpret_cast<int32_t *>(smem);
+#pragma unroll
+            for (int c = 0; c < BNT; ++c) red[c * C::BM + nl] = sums[c];
           }
         }
       }
-    } else {
-      // split-K: partial tile -> own shared memory, column-major [token][channel]
-      float *red = reinterpret_cast<float *>(smem);
-#pragma unroll 1
-      for (int c = 0; c < BNT; c += 16) {
-        uint32_t r[16];
-        if (run) {
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c, r);
-          tmem_ld_wait();
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) red[(c + j) * C::BM + nl] = run ? __uint_as_float(r[j]) : 0.0f;
-      }
     }
+    if (!ok) *abort_flag = 1;
   }
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, QLIN_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (S > 1) {
-    cluster_sync();  // every CTA of the cluster has written its partial tile
+  if (S > 1) {  // one unit per CTA: sum the partial tiles of the cluster
+    cluster_sync();
     if (warp >= 4) {
-      const int ct = threadIdx.x - 128;
+      const int ct = threadIdx.x - 128;  // 512 threads
       const uint32_t base = smem_u32(smem);
-      constexpr int U = BNT * C::BM / 4;  // float4 units of the tile
+      const int u = blockIdx.x, n0 = (u % p.ntiles) * C::BM, m0 = (u / p.ntiles) * BNT;
+      constexpr int U = BNT * C::BM / 4;  // 4-word units of the tile
       const int u0 = (int)((int64_t)split * U / S), u1 = (int)((int64_t)(split + 1) * U / S);
-      for (int u = u0 + ct; u < u1; u += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w4 = u0 + ct; w4 < u1; w4 += 512) {
+        uint32_t acc[4] = {0, 0, 0, 0};
         for (int r = 0; r < S; ++r) {  // fixed order: deterministic
-          const uint4 v = ld_dsmem_v4(map_peer_smem(base + 16u * u, (uint32_t)r));
-          acc.x += __uint_as_float(v.x);
-          acc.y += __uint_as_float(v.y);
-          acc.z += __uint_as_float(v.z);
-          acc.w += __uint_as_float(v.w);
-        }
-        const int e = 4 * u, j = e / C::BM, nl = e % C::BM;
-        const int m = m0 + j, n = n0 + nl;
-        if (m < p.M && n < p.N) {
-          float v[4] = {acc.x, acc.y, acc.z, acc.w};
-          uint32_t o[2];
+          const uint4 v = ld_dsmem_v4(map_peer_smem(base + 16u * w4, (uint32_t)r));
+          const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float a0 = v[2 * h] * __ldg(p.w_scale + n + 2 * h);
-            float a1 = v[2 * h + 1] * __ldg(p.w_scale + n + 2 * h + 1);
-            if (p.bias) {
-              a0 += bf16_bits_to_f32(__ldg(p.bias + n + 2 * h));
-              a1 += bf16_bits_to_f32(__ldg(p.bias + n + 2 * h + 1));
-            }
-            o[h] = pack_bf16x2(a0, a1);
-          }
-          *reinterpret_cast<uint2 *>(p.y + (size_t)m * p.N + n) = make_uint2(o[0], o[1]);
+          for (int e = 0; e < 4; ++e)
+            acc[e] = kI8 ? (uint32_t)((int32_t)acc[e] + (int32_t)vv[e])
+                         : __float_as_uint(__uint_as_float(acc[e]) + __uint_as_float(vv[e]));
         }
+        const int e0 = 4 * w4, jj = e0 / C::BM, nl = e0 % C::BM;
+        const int m = m0 + jj, n = n0 + nl;
+        if (m < p.M && n < p.N) store4<MODE>(p, m, n, acc);
       }
     }
     cluster_sync();  // no CTA leaves while a peer may still read its shared memory
   }
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ================================================================ launchers
@@ -470,9 +612,11 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
 int w8_swap_bnt(int64_t M) {
   return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
 }
+int i8_swap_bnt(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
-int w8_swap_splits(int64_t M, int64_t K, int64_t N, int sms) {
-  const int64_t tiles = ((N + 127) / 128) * ((M + w8_swap_bnt(M) - 1) / w8_swap_bnt(M));
+// Split-K factor: CTAs of a cluster that share one output tile when the tiles
+// alone cannot fill the GPU.
+int w8_swap_splits(int64_t tiles, int64_t K, int sms) {
   const int64_t kb = (K + 63) / 64;
   if (tiles * 4 >= (int64_t)sms * 3) return 1;
   int64_t s = sms / tiles;
@@ -481,20 +625,23 @@ int w8_swap_splits(int64_t M, int64_t K, int64_t N, int sms) {
   return s < 1 ? 1 : (int)s;
 }
 
-template <int BNT, int QT>
-static cudaError_t launch_swap_t(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
-  using C = SwapCfg<BNT>;
+template <int BNT, int QT, int MODE>
+static cudaError_t launch_dq_t(const GemmArgs &g, const void *xb, const DeviceInfo &dev, cudaStream_t st) {
+  using C = DqCfg<BNT>;
   CUtensorMap tw, tx;
-  if (!make_map(&tw, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.N, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&tx, g.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_map(&tw, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.N, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&tx, xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static cudaError_t attr = set_smem(k_w8_swap<BNT, QT>, C::SMEM);
+  static cudaError_t attr = set_smem(k_w8_dq<BNT, QT, MODE>, C::SMEM);
   if (attr != cudaSuccess) return attr;
-  const int S = w8_swap_splits(g.M, g.K, g.N, dev.sms);
-  SwapParams p{(int)g.M, (int)g.N, (int)g.K, S, g.w_scale, g.bias, (uint16_t *)g.y, dev.status};
+  const int ntiles = (int)((g.N + C::BM - 1) / C::BM);
+  const int units = ntiles * (int)((g.M + BNT - 1) / BNT);
+  const int S = w8_swap_splits(units, g.K, dev.sms);
+  const int G = S > 1 ? units : (units < dev.sms ? units : dev.sms);
+  SwapParams p{(int)g.M, (int)g.N, (int)g.K, S, units, ntiles, g.w_scale, g.x_scale, g.bias, g.y, dev.status};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((g.N + C::BM - 1) / C::BM), (unsigned)((g.M + BNT - 1) / BNT), (unsigned)S);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((unsigned)G, 1, (unsigned)S);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attrs[1];
@@ -504,25 +651,42 @@ static cudaError_t launch_swap_t(const GemmArgs &g, const DeviceInfo &dev, cudaS
   attrs[0].val.clusterDim.z = (unsigned)S;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_w8_swap<BNT, QT>, tw, tx, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_w8_dq<BNT, QT, MODE>, tw, tx, p);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int QT>
-static cudaError_t launch_swap_q(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
+static cudaError_t launch_w8a16_q(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
   switch (w8_swap_bnt(g.M)) {
-    case 16: return launch_swap_t<16, QT>(g, dev, st);
-    case 32: return launch_swap_t<32, QT>(g, dev, st);
-    case 64: return launch_swap_t<64, QT>(g, dev, st);
-    case 128: return launch_swap_t<128, QT>(g, dev, st);
-    default: return launch_swap_t<256, QT>(g, dev, st);
+    case 16: return launch_dq_t<16, QT, kSwapW8A16>(g, g.a, dev, st);
+    case 32: return launch_dq_t<32, QT, kSwapW8A16>(g, g.a, dev, st);
+    case 64: return launch_dq_t<64, QT, kSwapW8A16>(g, g.a, dev, st);
+    case 128: return launch_dq_t<128, QT, kSwapW8A16>(g, g.a, dev, st);
+    default: return launch_dq_t<256, QT, kSwapW8A16>(g, g.a, dev, st);
   }
 }
 
 cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
   if (g.M == 0) return cudaSuccess;
-  return g.qtype == QLIN_INT8 ? launch_swap_q<QLIN_INT8>(g, dev, st) : launch_swap_q<QLIN_E4M3>(g, dev, st);
+  return g.qtype == QLIN_INT8 ? launch_w8a16_q<QLIN_INT8>(g, dev, st) : launch_w8a16_q<QLIN_E4M3>(g, dev, st);
+}
+
+// INT8 x INT8 on the BF16 tensor cores; `xb` holds the activation codes as
+// integer-valued BF16 [M, K].  raw: int32 accumulator out; else scaled BF16.
+cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st) {
+  if (g.M == 0) return cudaSuccess;
+  switch (i8_swap_bnt(g.M)) {
+    case 16:
+      return raw ? launch_dq_t<16, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)
+                 : launch_dq_t<16, QLIN_INT8, kSwapI8Scaled>(g, xb, dev, st);
+    case 32:
+      return raw ? launch_dq_t<32, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)
+                 : launch_dq_t<32, QLIN_INT8, kSwapI8Scaled>(g, xb, dev, st);
+    default:
+      return raw ? launch_dq_t<64, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)
+                 : launch_dq_t<64, QLIN_INT8, kSwapI8Scaled>(g, xb, dev, st);
+  }
 }
 
 }  // namespace qlin

@@ -46,8 +46,15 @@ cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStrea
 // tcgen05 kernels (gemm_tc.cu)
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
+cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st);
 int w8_swap_bnt(int64_t M);
-int w8_swap_splits(int64_t M, int64_t K, int64_t N, int sms);
+int i8_swap_bnt(int64_t M);
+int w8_swap_splits(int64_t tiles, int64_t K, int sms);
+
+// INT8 operand preparation for the tensor-core INT8 path (quant_kernels.cu)
+cudaError_t launch_quantize_act_i8bf16(int64_t M, int64_t K, const void *x, const float *s, void *out, int sms,
+                                       cudaStream_t st);
+cudaError_t launch_i8_to_bf16(int64_t M, int64_t K, const void *q, void *out, int sms, cudaStream_t st);
 
 cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
                               cudaStream_t st);

@@ -74,20 +74,29 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_W8A16_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
-      static const char *names[5] = {"k_w8_swap<16>", "k_w8_swap<32>", "k_w8_swap<64>", "k_w8_swap<128>",
-                                     "k_w8_swap<256>"};
+      static const char *names[5] = {"k_w8_dq<16>", "k_w8_dq<32>", "k_w8_dq<64>", "k_w8_dq<128>", "k_w8_dq<256>"};
       const int b = w8_swap_bnt(M);
       return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : b == 128 ? 3 : 4];
     }
-    case QLIN_OP_I8_GEMM_S32:
+    case QLIN_OP_I8_GEMM_S32: {
       if (check_linear_shape(M, K, N)) return "invalid";
-      return M == 0 ? "none" : "k_gemm_simt";
-    case QLIN_OP_W8A8_LINEAR:
+      if (M == 0) return "none";
+      static const char *names[3] = {"k_i8_to_bf16+k_w8_dq<16,i8>", "k_i8_to_bf16+k_w8_dq<32,i8>",
+                                     "k_i8_to_bf16+k_w8_dq<64,i8>"};
+      const int b = i8_swap_bnt(M);
+      return names[b == 16 ? 0 : b == 32 ? 1 : 2];
+    }
+    case QLIN_OP_W8A8_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
       if (qtype == QLIN_E4M3) return (N % 256 == 0 || N > 1024) ? "k_quantize_act+k_fp8_gemm<256>"
                                                                   : "k_quantize_act+k_fp8_gemm<128>";
-      return "k_quantize_act+k_gemm_simt";
+      static const char *names[3] = {"k_quantize_act_i8bf16+k_w8_dq<16,i8>",
+                                     "k_quantize_act_i8bf16+k_w8_dq<32,i8>",
+                                     "k_quantize_act_i8bf16+k_w8_dq<64,i8>"};
+      const int b = i8_swap_bnt(M);
+      return names[b == 16 ? 0 : b == 32 ? 1 : 2];
+    }
   }
   return "invalid";
 }
@@ -111,8 +120,9 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     case QLIN_OP_ACT_SCALE: return 256;
     case QLIN_OP_QUANTIZE_ACT: return 0;
     case QLIN_OP_W8A16_LINEAR: return 0;
-    case QLIN_OP_W8A8_LINEAR: return round_up((size_t)M * (size_t)K, 256);
-    case QLIN_OP_I8_GEMM_S32: return 0;
+    // quantized activations: E4M3 codes (1 byte), or INT8 codes as integer-valued BF16 (2 bytes)
+    case QLIN_OP_W8A8_LINEAR: return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256);
+    case QLIN_OP_I8_GEMM_S32: return round_up((size_t)M * (size_t)K * 2, 256);
   }
   return (size_t)-1;
 }
@@ -185,10 +195,13 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
   if (qlin_status s = current_device(&dev)) return s;
   if (M == 0) return QLIN_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaError_t e = launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st)) return QLIN_ERR_CUDA;
   GemmArgs g{kW8A8, qtype, M, K, N, ws, qw, w_scale, input_scale, (const uint16_t *)bias, y};
-  if (qtype == QLIN_E4M3) return from_cuda(launch_fp8_gemm(g, *dev, st));
-  return from_cuda(launch_gemm_simt(g, *dev, st));
+  if (qtype == QLIN_E4M3) {
+    if (launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
+    return from_cuda(launch_fp8_gemm(g, *dev, st));
+  }
+  if (launch_quantize_act_i8bf16(M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
+  return from_cuda(launch_i8_swap(g, ws, false, *dev, st));
 }
 
 qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, const void *qw,
@@ -201,8 +214,10 @@ qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, co
   DeviceInfo *dev;
   if (qlin_status s = current_device(&dev)) return s;
   if (M == 0) return QLIN_OK;
-  GemmArgs g{kI8Raw, QLIN_INT8, M, K, N, qx, qw, nullptr, nullptr, nullptr, acc};
-  return from_cuda(launch_gemm_simt(g, *dev, (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_i8_to_bf16(M, K, qx, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
+  GemmArgs g{kI8Raw, QLIN_INT8, M, K, N, ws, qw, nullptr, nullptr, nullptr, acc};
+  return from_cuda(launch_i8_swap(g, ws, true, *dev, st));
 }
 
 qlin_status qlin_get_device_status(qlin_stream_t stream) {

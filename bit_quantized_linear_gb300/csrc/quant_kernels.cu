@@ -108,6 +108,48 @@ __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ 
   }
 }
 
+// ---------------------------------------------------------------------------
+// INT8 activation codes written as integer-valued BF16 (exact for |q| <= 127):
+// the B operand of the INT8 tensor-core path.  8 BF16 in, 8 BF16 codes out.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quantize_act_i8bf16(const uint4 *__restrict__ x,
+                                                            const float *__restrict__ s_ptr,
+                                                            uint4 *__restrict__ q, int64_t n8) {
+  const float s = __ldg(s_ptr);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 a = __ldg(x + i);
+    uint32_t in[4] = {a.x, a.y, a.z, a.w}, out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(in[j] & 0xFFFFu), s);
+      const float hi = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(in[j] >> 16), s);
+      out[j] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+    }
+    q[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// INT8 codes -> integer-valued BF16 (exact).  16 codes in, 16 BF16 out.
+__global__ void __launch_bounds__(256) k_i8_to_bf16(const uint4 *__restrict__ q, uint4 *__restrict__ out,
+                                                   int64_t n16) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 a = __ldg(q + i);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float lo = (float)(int8_t)(w[j] >> (16 * h));
+        const float hi = (float)(int8_t)(w[j] >> (16 * h + 8));
+        o[2 * j + h] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+      }
+    }
+    out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // --------------------------------- launchers --------------------------------
 static int stream_grid(int64_t work, int per_cta, int sms) {
   int64_t g = (work + per_cta - 1) / per_cta;
@@ -154,4 +196,23 @@ cudaError_t launch_quantize_act(int qtype, int64_t M, int64_t K, const void *x, 
   return cudaGetLastError();
 }
 
+}  // namespace qlin
+
+namespace qlin {
+cudaError_t launch_quantize_act_i8bf16(int64_t M, int64_t K, const void *x, const float *s, void *out, int sms,
+                                       cudaStream_t st) {
+  const int64_t n8 = M * K / 8;
+  if (n8 == 0) return cudaSuccess;
+  k_quantize_act_i8bf16<<<stream_grid(n8, 256, sms), 256, 0, st>>>((const uint4 *)x, s, (uint4 *)out, n8);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_i8_to_bf16(int64_t M, int64_t K, const void *q, void *out, int sms, cudaStream_t st) {
+  const int64_t n16 = M * K / 16;
+  if (n16 == 0) return cudaSuccess;
+  k_i8_to_bf16<<<stream_grid(n16, 256, sms), 256, 0, st>>>((const uint4 *)q, (uint4 *)out, n16);
+  note_launches(1);
+  return cudaGetLastError();
+}
 }  // namespace qlin

@@ -59,14 +59,18 @@ def test_noalloc_matches_workspace_entry_point_twice(capi, qt):
 
 
 def test_noalloc_rejects_sizes_beyond_scratch(capi):
+    """The largest M whose workspace fits the scratch is accepted by the size
+    check; one row more is refused with QLIN_ERR_WORKSPACE before any launch."""
     L = capi.lib()
     limit = capi.W8A8_NOALLOC_SCRATCH_BYTES
     src = open(os.path.join(ROOT, "include", "qlin.h")).read()
     assert re.search(r"QLIN_W8A8_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)32 << 20\)", src)
-    K = 4096
-    M = limit // K + 1  # one row too many
+    K, N = 4096, 256
     p = ctypes.c_void_p(4096)  # never dereferenced: refused before any launch
-    st = L.qlin_w8a8_linear_noalloc(0, M, K, 256, p, p, p, p, None, p,
-                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    assert st == capi.QLIN_ERR_WORKSPACE
-    assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A8_LINEAR, "int8", M - 1, K, 256) <= limit
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for qt in ("int8", "e4m3"):
+        need = lambda M: capi.qlin_workspace_bytes(capi.QLIN_OP_W8A8_LINEAR, qt, M, K, N)
+        m_max = limit // need(1)
+        assert need(m_max) <= limit < need(m_max + 1)
+        st = L.qlin_w8a8_linear_noalloc(capi.QTYPES[qt], m_max + 1, K, N, p, p, p, p, None, p, stream)
+        assert st == capi.QLIN_ERR_WORKSPACE
