@@ -60,6 +60,14 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel in the
+// stream is still running; pdl_wait() blocks until that kernel has completed
+// and its memory is visible (a no-op without the attribute).  pdl_trigger()
+// lets the next kernel start its own prologue early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Sets the device status word (first error wins).
 __device__ __forceinline__ void set_status(unsigned *status, unsigned code) {
   if (status) atomicCAS(status, 0u, code);

@@ -121,6 +121,8 @@ cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &, cudaStream_t
 
 // Failure-detection check kernel: waits on a flag with a global-time limit.
 __global__ void k_debug_wait(const volatile uint32_t *flag, uint64_t timeout_ns, unsigned *status) {
+  pdl_wait();
+  pdl_trigger();
   const uint64_t t0 = globaltimer_ns();
   while (*flag == 0u) {
     if (globaltimer_ns() - t0 > timeout_ns) {
@@ -133,9 +135,7 @@ __global__ void k_debug_wait(const volatile uint32_t *flag, uint64_t timeout_ns,
 
 cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
                               cudaStream_t st) {
-  k_debug_wait<<<1, 1, 0, st>>>(flag, timeout_ns, status);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_kernel(k_debug_wait, dim3(1), dim3(1), 0, st, 1, (const volatile uint32_t *)flag, timeout_ns, status);
 }
 
 }  // namespace qlin

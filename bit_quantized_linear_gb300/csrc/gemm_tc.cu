@@ -123,6 +123,8 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
+  pdl_trigger();
 
   if (warp == 0 && lane == 0) {  // ---------------- TMA producer
     for (int i = 0; i < nkb; ++i) {
@@ -239,14 +241,20 @@ struct DqCfg {
   static constexpr int R = R0 > 16 ? 16 : R0;
   static constexpr int X_OFF = 0, RAW_OFF = X * X_BYTES, BAR_OFF = RAW_OFF + R * RAW_BYTES;
   static constexpr int SMEM = BAR_OFF + 1024 + 1024;  // alignment slack + barriers
-  static constexpr int ND = BNT <= 128 ? 2 : 1;        // accumulator buffers in TMEM
-  static constexpr int DSTRIDE = BNT <= 64 ? 64 : BNT;
-  static constexpr int ACOL = BNT <= 64 ? 128 : 256;   // first TMEM column of the A ring
-  static constexpr int NA = BNT <= 64 ? 12 : 8;        // A stages, 32 columns (64 BF16 k) each
-  static constexpr int QUADS = 3;                      // converter warp quads
-  static constexpr int THREADS = 640;                  // 20 warps
+  // Accumulators.  A chain of MMAs into one small tile is bound by the MMA's
+  // accumulate latency, not its throughput, so consecutive k-blocks rotate
+  // over NACC independent accumulator tiles (summed in a fixed order by the
+  // epilogue); ND sets of them alternate between consecutive output tiles.
+  static constexpr int NACC = BNT <= 32 ? 4 : BNT <= 128 ? 2 : 1;
+  static constexpr int DSTRIDE = NACC * BNT;                // columns of one accumulator set
+  static constexpr int ND = 2 * DSTRIDE <= 256 ? 2 : 1;
+  static constexpr int ACOL = ND * DSTRIDE <= 128 ? 128 : 256;  // first TMEM column of the A ring
+  static constexpr int NA = (512 - ACOL) / 32 > 12 ? 12 : (512 - ACOL) / 32;  // A stages, 32 columns each
+  static constexpr int QUADS = 3;                           // converter warp quads
+  static constexpr int ISSUERS = NACC >= 2 ? 2 : 1;         // MMA-issuing threads (own accumulators each)
+  static constexpr int THREADS = 640;                       // 20 warps
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
-  static_assert(ACOL + NA * 32 <= 512, "TMEM columns");
+  static_assert(ND * DSTRIDE <= ACOL && ACOL + NA * 32 <= 512, "TMEM columns");
   static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(2 * (R + X + NA + ND) * 8 + 16 <= 1024, "barrier area");
@@ -350,8 +358,8 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < C::ND; ++s) {
-      mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 4);  // the epilogue quad
+      mbar_init(&acc_full[s], C::ISSUERS);  // one commit per MMA issuer
+      mbar_init(&acc_empty[s], 4);          // the epilogue quad
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -363,64 +371,82 @@ __global__ void __launch_bounds__(640, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
+  pdl_trigger();
 
   if (warp == 0) {  // ------------------------ weight-tile producer
     if (lane == 0) {
-      for (int i = 0; i < total; ++i) {
-        const int j = i / nkb, kb = i - j * nkb, s = i % C::R;
-        if (i >= C::R && !mbar_wait(&raw_empty[s], ((i / C::R) & 1) ^ 1, abort_flag)) {
-          *abort_flag = 1;
-          break;
+      int i = 0;
+      for (int j = 0; j < my_units && !*abort_flag; ++j) {
+        const int n0 = ((blockIdx.x + j * G) % p.ntiles) * C::BM;
+        for (int kb = 0; kb < nkb; ++kb, ++i) {
+          const int s = i % C::R;
+          if (i >= C::R && !mbar_wait(&raw_empty[s], ((i / C::R) & 1) ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[s], C::RAW_BYTES);
+          tma_load_2d(&tm_w, &raw_full[s], raws + s * C::RAW_BYTES, (kb0 + kb) * C::BK, n0);
         }
-        const int u = blockIdx.x + j * G;
-        mbar_arrive_expect_tx(&raw_full[s], C::RAW_BYTES);
-        tma_load_2d(&tm_w, &raw_full[s], raws + s * C::RAW_BYTES, (kb0 + kb) * C::BK, (u % p.ntiles) * C::BM);
       }
     }
   } else if (warp == 2) {  // ----------------- activation-tile producer
     if (lane == 0) {
-      for (int i = 0; i < total; ++i) {
-        const int j = i / nkb, kb = i - j * nkb, s = i % C::X;
-        if (i >= C::X && !mbar_wait(&x_empty[s], ((i / C::X) & 1) ^ 1, abort_flag)) {
-          *abort_flag = 1;
-          break;
+      int i = 0;
+      for (int j = 0; j < my_units && !*abort_flag; ++j) {
+        const int m0 = ((blockIdx.x + j * G) / p.ntiles) * BNT;
+        for (int kb = 0; kb < nkb; ++kb, ++i) {
+          const int s = i % C::X;
+          if (i >= C::X && !mbar_wait(&x_empty[s], ((i / C::X) & 1) ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&x_full[s], C::X_BYTES);
+          tma_load_2d(&tm_x, &x_full[s], xs + s * C::X_BYTES, (kb0 + kb) * C::BK, m0);
         }
-        const int u = blockIdx.x + j * G;
-        mbar_arrive_expect_tx(&x_full[s], C::X_BYTES);
-        tma_load_2d(&tm_x, &x_full[s], xs + s * C::X_BYTES, (kb0 + kb) * C::BK, (u / p.ntiles) * BNT);
       }
     }
-  } else if (warp == 1) {  // ----------------- MMA issuer
+  } else if (warp == 1 || (warp == 3 && C::ISSUERS == 2)) {  // -- MMA issuers
+    // Issuer e (warp 1: e = 0, warp 3: e = 1) takes the k-blocks with kb % ISSUERS == e
+    // and accumulates them into its own accumulator tiles (kb % NACC).  The MMA
+    // instructions of a block are straight-line code followed by unconditional
+    // commits: that keeps one thread issuing an MMA every few dozen cycles.
     if (lane == 0) {
+      const int e = warp == 1 ? 0 : 1;
       bool ok = true;
-      int cidx = 0;
-      for (int i = 0; i < total && ok; ++i) {
-        const int kb = i % nkb;
-        const bool cstart = (kb % CH) == 0;
-        const bool cend = (kb % CH) == CH - 1 || kb == nkb - 1;
-        const int db = cidx % C::ND;
-        if (cstart && cidx >= C::ND) {
-          if (!mbar_wait(&acc_empty[db], ((cidx / C::ND) & 1) ^ 1, abort_flag)) {
+      int cidx = 0;  // chunk counter (same sequence as the epilogue's)
+      for (int j = 0; j < my_units && ok; ++j) {
+        for (int cb = 0; cb < nkb && ok; cb += CH, ++cidx) {  // chunk = k-blocks [cb, ce)
+          const int ce = min(nkb, cb + CH);
+          const int db = cidx % C::ND;
+          if (cidx >= C::ND && !mbar_wait(&acc_empty[db], ((cidx / C::ND) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-        }
-        const int sx = i % C::X, sa = i % C::NA;
-        if (!mbar_wait(&x_full[sx], (i / C::X) & 1, abort_flag) || !mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t dt = tmem + db * C::DSTRIDE, at = tmem + C::ACOL + sa * 32;
-        const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::X_BYTES));
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)  // K = 16 per instruction: 8 TMEM columns of A, 32 bytes of B
-          mma_bf16_ts(dt, at + 8 * kk, bd + 2 * kk, C::IDESC, (!cstart || kk > 0) ? 1u : 0u);
-        mma_commit(&x_empty[sx]);
-        mma_commit(&a_empty[sa]);
-        if (cend) {
-          mma_commit(&acc_full[db]);
-          ++cidx;
+          tc_fence_after();
+          const uint32_t dset = tmem + db * C::DSTRIDE;
+          for (int kb = cb + e; kb < ce; kb += C::ISSUERS) {
+            const int i = j * nkb + kb;  // block index within this CTA
+            const int sx = i % C::X, sa = i % C::NA;
+            if (!mbar_wait(&x_full[sx], (i / C::X) & 1, abort_flag) ||
+                !mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int rel = kb - cb;
+            const uint32_t dt = dset + (rel % C::NACC) * BNT, at = tmem + C::ACOL + sa * 32;
+            const uint32_t acc0 = rel < C::NACC ? 0u : 1u;  // first block of its accumulator starts it
+            const uint64_t bd = umma_desc_sw128(smem_u32(xs + sx * C::X_BYTES));
+            mma_bf16_ts(dt, at, bd, C::IDESC, acc0);
+            mma_bf16_ts(dt, at + 8, bd + 2, C::IDESC, 1u);
+            mma_bf16_ts(dt, at + 16, bd + 4, C::IDESC, 1u);
+            mma_bf16_ts(dt, at + 24, bd + 6, C::IDESC, 1u);
+            mma_commit(&x_empty[sx]);
+            mma_commit(&a_empty[sa]);
+          }
+          if (!ok) break;
+          mma_commit(&acc_full[db]);  // arrives when this issuer's MMAs of the chunk are done
         }
       }
       if (!ok) *abort_flag = 1;
@@ -481,14 +507,31 @@ __global__ void __launch_bounds__(640, 1)
           break;
         }
         const uint32_t dt = tmem + lane_base + db * C::DSTRIDE;
-        if constexpr (kI8) {
-#pragma unroll
-          for (int c = 0; c < BNT; c += 16) {
-            uint32_t r[16];
-            tmem_ld16(dt + c, r);
+        const int in_chunk = min(CH, nkb - ch * CH);
+        const int nacc = in_chunk < C::NACC ? in_chunk : C::NACC;  // accumulators written in this chunk
+        // 16 columns of the chunk's sum: accumulators added in a fixed order
+        auto load16 = [&](int c, uint32_t (&r)[16]) {
+          tmem_ld16(dt + c, r);
+          tmem_ld_wait();
+          for (int a = 1; a < nacc; ++a) {
+            uint32_t t[16];
+            tmem_ld16(dt + a * BNT + c, t);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sums[c + e] += __float2int_rn(__uint_as_float(r[e]));
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(t[e]));
+          }
+        };
+        if constexpr (kI8) {
+          // each accumulator holds an exact integer below 2^23: convert, then add in int32
+          for (int a = 0; a < nacc; ++a) {
+#pragma unroll
+            for (int c = 0; c < BNT; c += 16) {
+              uint32_t r[16];
+              tmem_ld16(dt + a * BNT + c, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) sums[c + e] += __float2int_rn(__uint_as_float(r[e]));
+            }
           }
         } else if (S == 1) {
           const float sw = valid ? __ldg(p.w_scale + n) : 0.0f;
@@ -497,8 +540,7 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll 1
           for (int c = 0; c < BNT; c += 16) {
             uint32_t r[16];
-            tmem_ld16(dt + c, r);
-            tmem_ld_wait();
+            load16(c, r);
             if (valid) {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
@@ -512,8 +554,7 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll 1
           for (int c = 0; c < BNT; c += 16) {
             uint32_t r[16];
-            tmem_ld16(dt + c, r);
-            tmem_ld_wait();
+            load16(c, r);
 #pragma unroll
             for (int e = 0; e < 16; ++e) red[(c + e) * C::BM + nl] = r[e];
           }
@@ -598,9 +639,7 @@ static cudaError_t launch_fp8_bn(const GemmArgs &g, const DeviceInfo &dev, cudaS
   if (attr != cudaSuccess) return attr;
   Fp8Params p{(int)g.M, (int)g.N, (int)g.K, g.w_scale, g.x_scale, g.bias, (uint16_t *)g.y, dev.status};
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + C::BM - 1) / C::BM));
-  k_fp8_gemm<BN><<<grid, 256, C::SMEM, st>>>(ta, tb, p);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_kernel(k_fp8_gemm<BN>, grid, dim3(256), C::SMEM, st, 1, ta, tb, p);
 }
 
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
@@ -639,21 +678,8 @@ static cudaError_t launch_dq_t(const GemmArgs &g, const void *xb, const DeviceIn
   const int S = w8_swap_splits(units, g.K, dev.sms);
   const int G = S > 1 ? units : (units < dev.sms ? units : dev.sms);
   SwapParams p{(int)g.M, (int)g.N, (int)g.K, S, units, ntiles, g.w_scale, g.x_scale, g.bias, g.y, dev.status};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)G, 1, (unsigned)S);
-  cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = 1;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = (unsigned)S;
-  cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_w8_dq<BNT, QT, MODE>, tw, tx, p);
-  note_launches(1);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_kernel(k_w8_dq<BNT, QT, MODE>, dim3((unsigned)G, 1, (unsigned)S), dim3(C::THREADS), C::SMEM, st,
+                       (unsigned)S, tw, tx, p);
 }
 
 template <int QT>

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace qlin {
 
 struct DeviceInfo {
@@ -14,6 +16,36 @@ struct DeviceInfo {
 
 // Host-side count of kernels enqueued by the library (qlin_launch_count).
 void note_launches(int n);
+
+// Launches `kernel` on `st` with programmatic stream serialization (the kernel
+// calls pdl_wait() before reading global inputs) and an optional cluster
+// shape along z.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          unsigned cluster_z, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster_z > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = cluster_z;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_quantize_weight(int qtype, int64_t N, int64_t K, const float *w, void *qw,
                                    float *s, cudaStream_t st);

@@ -16,6 +16,8 @@ template <int QT>
 __global__ void __launch_bounds__(256) k_quantize_weight(const float *__restrict__ w,
                                                          uint8_t *__restrict__ q,
                                                          float *__restrict__ s, int64_t K) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8];
   const int64_t n = blockIdx.x;
   const float4 *row = reinterpret_cast<const float4 *>(w + n * K);
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(256) k_quantize_weight(const float *__restrict
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_absmax_bf16(const uint4 *__restrict__ x, int64_t n8,
                                                      unsigned *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8];
   float amax = 0.0f;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
@@ -78,6 +82,8 @@ __global__ void __launch_bounds__(256) k_absmax_bf16(const uint4 *__restrict__ x
 
 __global__ void k_scale_finalize(const unsigned *__restrict__ amax_bits, float *__restrict__ scale,
                                  float qmax) {
+  pdl_wait();
+  pdl_trigger();
   const float a = __uint_as_float(*amax_bits);
   *scale = a > 0.0f ? __fdiv_rn(a, qmax) : 1.0f;
 }
@@ -90,6 +96,8 @@ template <int QT>
 __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ x,
                                                       const float *__restrict__ s_ptr,
                                                       uint4 *__restrict__ q, int64_t n16) {
+  pdl_wait();
+  pdl_trigger();
   const float s = __ldg(s_ptr);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -115,6 +123,8 @@ __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ 
 __global__ void __launch_bounds__(256) k_quantize_act_i8bf16(const uint4 *__restrict__ x,
                                                             const float *__restrict__ s_ptr,
                                                             uint4 *__restrict__ q, int64_t n8) {
+  pdl_wait();
+  pdl_trigger();
   const float s = __ldg(s_ptr);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
     const uint4 a = __ldg(x + i);
@@ -132,6 +142,8 @@ __global__ void __launch_bounds__(256) k_quantize_act_i8bf16(const uint4 *__rest
 // INT8 codes -> integer-valued BF16 (exact).  16 codes in, 16 BF16 out.
 __global__ void __launch_bounds__(256) k_i8_to_bf16(const uint4 *__restrict__ q, uint4 *__restrict__ out,
                                                    int64_t n16) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
     const uint4 a = __ldg(q + i);
     const uint32_t w[4] = {a.x, a.y, a.z, a.w};
@@ -162,12 +174,9 @@ cudaError_t launch_quantize_weight(int qtype, int64_t N, int64_t K, const float 
                                    float *s, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
   dim3 grid((unsigned)N), block(256);
-  if (qtype == QLIN_INT8)
-    k_quantize_weight<QLIN_INT8><<<grid, block, 0, st>>>(w, (uint8_t *)qw, s, K);
-  else
-    k_quantize_weight<QLIN_E4M3><<<grid, block, 0, st>>>(w, (uint8_t *)qw, s, K);
-  note_launches(1);
-  return cudaGetLastError();
+  return qtype == QLIN_INT8
+             ? launch_kernel(k_quantize_weight<QLIN_INT8>, grid, block, 0, st, 1, w, (uint8_t *)qw, s, K)
+             : launch_kernel(k_quantize_weight<QLIN_E4M3>, grid, block, 0, st, 1, w, (uint8_t *)qw, s, K);
 }
 
 cudaError_t launch_act_scale(int qtype, int64_t rows, int64_t K, const void *x, float *scale,
@@ -175,12 +184,10 @@ cudaError_t launch_act_scale(int qtype, int64_t rows, int64_t K, const void *x, 
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * K / 8;
-  k_absmax_bf16<<<stream_grid(n8, 256 * 4, sms), 256, 0, st>>>((const uint4 *)x, n8, (unsigned *)ws);
-  e = cudaGetLastError();
+  e = launch_kernel(k_absmax_bf16, dim3(stream_grid(n8, 256 * 4, sms)), dim3(256), 0, st, 1, (const uint4 *)x, n8,
+                    (unsigned *)ws);
   if (e != cudaSuccess) return e;
-  k_scale_finalize<<<1, 1, 0, st>>>((const unsigned *)ws, scale, qmax_of(qtype));
-  note_launches(2);
-  return cudaGetLastError();
+  return launch_kernel(k_scale_finalize, dim3(1), dim3(1), 0, st, 1, (const unsigned *)ws, scale, qmax_of(qtype));
 }
 
 cudaError_t launch_quantize_act(int qtype, int64_t M, int64_t K, const void *x, const float *s,
@@ -188,12 +195,11 @@ cudaError_t launch_quantize_act(int qtype, int64_t M, int64_t K, const void *x, 
   const int64_t n16 = M * K / 16;
   if (n16 == 0) return cudaSuccess;
   const int grid = stream_grid(n16, 256, sms);
-  if (qtype == QLIN_INT8)
-    k_quantize_act<QLIN_INT8><<<grid, 256, 0, st>>>((const uint4 *)x, s, (uint4 *)qx, n16);
-  else
-    k_quantize_act<QLIN_E4M3><<<grid, 256, 0, st>>>((const uint4 *)x, s, (uint4 *)qx, n16);
-  note_launches(1);
-  return cudaGetLastError();
+  return qtype == QLIN_INT8
+             ? launch_kernel(k_quantize_act<QLIN_INT8>, dim3(grid), dim3(256), 0, st, 1, (const uint4 *)x, s,
+                             (uint4 *)qx, n16)
+             : launch_kernel(k_quantize_act<QLIN_E4M3>, dim3(grid), dim3(256), 0, st, 1, (const uint4 *)x, s,
+                             (uint4 *)qx, n16);
 }
 
 }  // namespace qlin
@@ -203,16 +209,14 @@ cudaError_t launch_quantize_act_i8bf16(int64_t M, int64_t K, const void *x, cons
                                        cudaStream_t st) {
   const int64_t n8 = M * K / 8;
   if (n8 == 0) return cudaSuccess;
-  k_quantize_act_i8bf16<<<stream_grid(n8, 256, sms), 256, 0, st>>>((const uint4 *)x, s, (uint4 *)out, n8);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_kernel(k_quantize_act_i8bf16, dim3(stream_grid(n8, 256, sms)), dim3(256), 0, st, 1,
+                       (const uint4 *)x, s, (uint4 *)out, n8);
 }
 
 cudaError_t launch_i8_to_bf16(int64_t M, int64_t K, const void *q, void *out, int sms, cudaStream_t st) {
   const int64_t n16 = M * K / 16;
   if (n16 == 0) return cudaSuccess;
-  k_i8_to_bf16<<<stream_grid(n16, 256, sms), 256, 0, st>>>((const uint4 *)q, (uint4 *)out, n16);
-  note_launches(1);
-  return cudaGetLastError();
+  return launch_kernel(k_i8_to_bf16, dim3(stream_grid(n16, 256, sms)), dim3(256), 0, st, 1, (const uint4 *)q,
+                       (uint4 *)out, n16);
 }
 }  // namespace qlin
