@@ -87,7 +87,7 @@ def load_peaks():
 
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -103,7 +103,7 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -225,6 +225,47 @@ class GpuWorkload:
         op = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR}
         self.kernel = [capi.qlin_kernel_name(op[l.form], l.qtype, l.M, l.K, l.N) for l in self.lins]
 
+    def _capture(self, copy, events=None, e2e=False):
+        """CUDA graph of one step on weight copy `copy` (PDL edges between the
+        kernels); with `events`, each call is bracketed by external event nodes;
+        with `e2e`, host->device copies of the activations and device->host
+        copies of the outputs are part of the graph."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            if e2e:
+                for i in range(len(self.lins)):
+                    self.x[i].copy_(self.x_host[i], non_blocking=True)
+            args = self.args[copy]
+            for i, fn in enumerate(self.fns):
+                if events is not None:
+                    events[i][0].record(self.stream)
+                st = fn(*args[i])
+                if events is not None:
+                    events[i][1].record(self.stream)
+                if st != 0:
+                    raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
+            if e2e:
+                for i in range(len(self.lins)):
+                    self.y_host[i].copy_(self.y[i], non_blocking=True)
+        return g
+
+    def build_graphs(self, with_events):
+        torch = self.torch
+        # capture on a side stream; the pre-marshalled stream argument must be the capture stream
+        self.stream = torch.cuda.Stream()
+        sp = ctypes.c_void_p(self.stream.cuda_stream)
+        self.args = [[a[:-1] + (sp,) for a in argset] for argset in self.args]
+        torch.cuda.synchronize()
+        self.graphs = [self._capture(c) for c in range(self.copies)]
+        self.graphs_e2e = [self._capture(c, e2e=True) for c in range(self.copies)]
+        self.events = None
+        if with_events:
+            self.events = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                            for _ in self.lins] for _ in range(self.copies)]
+            self.graphs_ev = [self._capture(c, events=self.events[c]) for c in range(self.copies)]
+        torch.cuda.synchronize()
+
     def run_step(self, step, ev=None):
         args = self.args[step % self.copies]
         for i, fn in enumerate(self.fns):
@@ -320,7 +361,7 @@ def cpu_baseline(name, unit_scale, unit):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     ap.add_argument("--workload", default="decode7b",
@@ -384,35 +425,59 @@ def main():
     for s in range(a.warmup):
         W.run_step(s)
     torch.cuda.synchronize()
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext_events = True
+    except TypeError:
+        ext_events = False
+    W.build_graphs(with_events=ext_events)
+    # graph replays launch on torch's current stream: make it the capture stream
+    stream_ctx = torch.cuda.stream(W.stream)
+    stream_ctx.__enter__()
+    for s in range(a.warmup):
+        W.graphs[s % W.copies].replay()
+    torch.cuda.synchronize()
 
-    # ---- device-timed region (inputs resident) ----
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n)]
-           for _ in range(a.steps)]
+    # ---- timed region 1: whole steps as CUDA-graph replays (inputs resident) ----
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = capi.qlin_launch_count()
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize()
         t_start.record(W.stream)
         for s in range(a.steps):
-            W.run_step(s, evs[s])
+            W.graphs[s % W.copies].replay()
         t_end.record(W.stream)
         torch.cuda.synchronize()
         barrier()
-    launches = capi.qlin_launch_count() - launches0
+    # graph replays do not pass through the host entry points: count the kernels a step launches
+    launches = sum(len(k.split("+")) for k in W.kernel) * a.steps
     elapsed = t_start.elapsed_time(t_end) / 1e3
     if world > 1:
         t = torch.tensor([elapsed], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed = float(t.item())
     clocks = clk.summary()
-    if torch.cuda.get_device_properties(dev).name and clocks.get("reasons") is None:
-        clocks["reasons"] = []
     ms_step = elapsed / a.steps * 1e3
     value = units_step * a.steps * world / elapsed / unit_scale
 
-    # per-call durations -> per-kernel attribution
-    dur = np.array([[evs[s][i][0].elapsed_time(evs[s][i][1]) / 1e3 for i in range(n)] for s in range(a.steps)])
+    # ---- timed region 2: per-launch durations (each call bracketed by CUDA events) ----
+    dur = np.zeros((a.steps, n))
+    if W.events is not None:
+        for s in range(a.steps):
+            W.graphs_ev[s % W.copies].replay()
+            torch.cuda.synchronize()
+            evs = W.events[s % W.copies]
+            dur[s] = [evs[i][0].elapsed_time(evs[i][1]) / 1e3 for i in range(n)]
+        timing = "graph replay with external event nodes around each launch"
+    else:
+        evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(n)]
+               for _ in range(a.steps)]
+        torch.cuda.synchronize()
+        for s in range(a.steps):
+            W.run_step(s, evs[s])
+        torch.cuda.synchronize()
+        dur = np.array([[evs[s][i][0].elapsed_time(evs[s][i][1]) / 1e3 for i in range(n)] for s in range(a.steps)])
+        timing = "stream events around each launch"
     mean_call = dur.mean(axis=0)
     per_kernel = {}
     for i, l in enumerate(W.lins):
@@ -438,6 +503,7 @@ def main():
     roof["traffic"] = tr
     roof["kernel"] = dom
     roof["peak_source"] = f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured" else "fallback"
+    roof["timing"] = timing
     # roofline time over the whole step: sum_i max(bytes_i / BW, flops_i / peak_i) / measured
     rt = 0.0
     for l in W.lins:
@@ -455,13 +521,13 @@ def main():
     e2e = None
     if not a.no_e2e:
         for s in range(a.warmup):
-            W.run_step_e2e(s)
+            W.graphs_e2e[s % W.copies].replay()
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(W.stream)
         for s in range(a.steps):
-            W.run_step_e2e(s)
+            W.graphs_e2e[s % W.copies].replay()
         e1.record(W.stream)
         torch.cuda.synchronize()
         et = e0.elapsed_time(e1) / 1e3
@@ -471,8 +537,10 @@ def main():
             et = float(t.item())
         e2e = {"value": units_step * a.steps * world / et / unit_scale, "unit": metric_unit,
                "h2d_bytes_per_step": int(sum(2 * l.M * l.K for l in W.lins)),
-               "d2h_bytes_per_step": int(sum(2 * l.M * l.N for l in W.lins))}
+               "d2h_bytes_per_step": int(sum(2 * l.M * l.N for l in W.lins)),
+               "how": "CUDA-graph replay: pinned-host activations copied in, the linears, outputs copied out"}
 
+    stream_ctx.__exit__(None, None, None)
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         cpu = cpu_baseline(a.workload, unit_scale, metric_unit)
@@ -489,7 +557,8 @@ def main():
                        "weight_bytes": W.weight_bytes, "weight_copies": W.copies,
                        "l2": (f"{W.copies} alternating weight copies of {W.weight_bytes / 1e6:.0f} MB each "
                               f"(L2 is {L2_BYTES / 2**20:.0f} MiB)"),
-                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                       "timing": "CUDA-graph replay of whole steps, CUDA events around the K steps"},
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
