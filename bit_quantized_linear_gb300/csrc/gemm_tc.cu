@@ -75,8 +75,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ============================================================ FP8 W8A8 GEMM
+// Persistent: each CTA walks output tiles t = blockIdx.x + j * gridDim.x
+// (128 tokens x 256 channels).  TMEM holds two 256-column fp32 accumulators,
+// so the epilogue of one tile overlaps the MMAs of the next.  Warps: 0 = TMA
+// producer, 1 = TMEM allocator + MMA issuer, 4..11 = epilogue (two quads, each
+// owning 128 of the tile's 256 channels).
 struct Fp8Params {
   int M, N, K;
+  int mtiles, ntiles;
   const float *w_scale;
   const float *x_scale;
   const uint16_t *bias;
@@ -84,41 +90,46 @@ struct Fp8Params {
   unsigned *status;
 };
 
-template <int BN>
 struct Fp8Cfg {
-  static constexpr int BM = 128, BK = 128, STAGES = 4;
+  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
   static constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int THREADS = 384;
   static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, BN);
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-template <int BN>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Fp8Params p) {
-  using C = Fp8Cfg<BN>;
+  using C = Fp8Cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint64_t *full = (uint64_t *)(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t *full = (uint64_t *)(smem + C::BAR_OFF);
   uint64_t *empty = full + C::STAGES;
-  uint64_t *acc_full = empty + C::STAGES;
-  uint32_t *tmem_slot = (uint32_t *)(acc_full + 1);
+  uint64_t *acc_full = empty + C::STAGES, *acc_empty = acc_full + 2;
+  uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * C::BM, n0 = blockIdx.x * BN;
   const int nkb = (p.K + C::BK - 1) / C::BK;
+  const int tiles = p.mtiles * p.ntiles, G = gridDim.x;
+  const int my_tiles = ((int)blockIdx.x < tiles) ? (tiles - (int)blockIdx.x + G - 1) / G : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);  // the eight epilogue warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, BN);
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -126,78 +137,111 @@ __global__ void __launch_bounds__(256, 1)
   pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
   pdl_trigger();
 
-  if (warp == 0 && lane == 0) {  // ---------------- TMA producer
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % C::STAGES;
-      if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      uint8_t *a = smem + s * C::STAGE_BYTES;
-      mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-      tma_load_2d(&tm_a, &full[s], a, i * C::BK, m0);
-      tma_load_2d(&tm_b, &full[s], a + C::A_BYTES, i * C::BK, n0);
-    }
-  } else if (warp == 1 && lane == 0) {  // ---------- MMA issuer
-    bool ok = true;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % C::STAGES;
-      if (!mbar_wait(&full[s], (i / C::STAGES) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t a = smem_u32(smem + s * C::STAGE_BYTES);
-      const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(a + C::A_BYTES);
-#pragma unroll
-      for (int kk = 0; kk < C::BK / 32; ++kk)  // K = 32 per instruction (32 bytes)
-        mma_fp8(tmem, ad + 2 * kk, bd + 2 * kk, C::IDESC, (i | kk) != 0);
-      mma_commit(&empty[s]);
-    }
-    if (!ok) *abort_flag = 1;
-    mma_commit(acc_full);
-  } else if (warp >= 4) {  // ------------------------ epilogue
-    const int q = warp & 3;
-    const int m = m0 + q * 32 + lane;
-    const bool ok = mbar_wait(acc_full, 0, abort_flag);
-    tc_fence_after();
-    // tcgen05.ld is warp-collective: every lane of the warp takes the same path
-    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
-      const float sx = __ldg(p.x_scale);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
-        tmem_ld_wait();
-        const int nb = n0 + c * 32;
-        if (m < p.M && nb < p.N) {
-          uint4 *dst = reinterpret_cast<uint4 *>(p.y + (size_t)m * p.N + nb);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (nb + 8 * g >= p.N) break;
-            uint32_t o[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int j = 8 * g + 2 * h;
-              float v0 = __uint_as_float(r[j]) * (sx * __ldg(p.w_scale + nb + j));
-              float v1 = __uint_as_float(r[j + 1]) * (sx * __ldg(p.w_scale + nb + j + 1));
-              if (p.bias) {
-                v0 += bf16_bits_to_f32(__ldg(p.bias + nb + j));
-                v1 += bf16_bits_to_f32(__ldg(p.bias + nb + j + 1));
-              }
-              o[h] = pack_bf16x2(v0, v1);
-            }
-            dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+  if (warp == 0) {  // ------------------------------- TMA producer
+    if (lane == 0) {
+      int i = 0;
+      for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
+        const int t = blockIdx.x + j * G;
+        const int m0 = (t / p.ntiles) * C::BM, n0 = (t % p.ntiles) * C::BN;
+        for (int kb = 0; kb < nkb; ++kb, ++i) {
+          const int s = i % C::STAGES;
+          if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            break;
           }
+          uint8_t *st = smem + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(&tm_a, &full[s], st, kb * C::BK, m0);
+          tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, n0);
         }
       }
     }
+  } else if (warp == 1) {  // ------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int i = 0;
+      for (int j = 0; j < my_tiles && ok; ++j) {
+        const int b = j & 1;
+        if (j >= 2 && !mbar_wait(&acc_empty[b], ((j >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem + b * C::BN;
+        for (int kb = 0; kb < nkb; ++kb, ++i) {
+          const int s = i % C::STAGES;
+          if (!mbar_wait(&full[s], (i / C::STAGES) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + s * C::STAGE_BYTES);
+          const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(a + C::A_BYTES);
+          mma_fp8(dt, ad, bd, C::IDESC, kb > 0 ? 1u : 0u);  // K = 32 per instruction (32 bytes)
+          mma_fp8(dt, ad + 2, bd + 2, C::IDESC, 1u);
+          mma_fp8(dt, ad + 4, bd + 4, C::IDESC, 1u);
+          mma_fp8(dt, ad + 6, bd + 6, C::IDESC, 1u);
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[b]);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp >= 4) {  // ------------------------- epilogue
+    const int q4 = warp & 3, half = (warp - 4) >> 2;  // half h owns channels [128h, 128h + 128)
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const float sx = __ldg(p.x_scale);
+    bool ok = true;
+    for (int j = 0; j < my_tiles && ok; ++j) {
+      const int t = blockIdx.x + j * G, b = j & 1;
+      const int m0 = (t / p.ntiles) * C::BM, n0 = (t % p.ntiles) * C::BN;
+      ok = mbar_wait(&acc_full[b], (j >> 1) & 1, abort_flag);
+      tc_fence_after();
+      // tcgen05.ld is warp-collective: every lane of the warp takes the same path
+      if (!__all_sync(0xffffffffu, ok && !*abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int m = m0 + q4 * 32 + lane;
+      uint16_t *yrow = p.y + (size_t)m * p.N;
+#pragma unroll 1
+      for (int c = 128 * half; c < 128 * half + 128; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + b * C::BN + c, r);
+        const int nb = n0 + c;
+        // column factors of this 32-column group: lane l holds column nb + l, shuffled below
+        const bool cv = nb + lane < p.N;
+        const float scl = cv ? sx * __ldg(p.w_scale + nb + lane) : 0.0f;
+        const float bia = (cv && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + nb + lane)) : 0.0f;
+        tmem_ld_wait();
+        uint32_t o[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float v0 = fmaf(__uint_as_float(r[2 * h]), __shfl_sync(0xffffffffu, scl, 2 * h),
+                                __shfl_sync(0xffffffffu, bia, 2 * h));
+          const float v1 = fmaf(__uint_as_float(r[2 * h + 1]), __shfl_sync(0xffffffffu, scl, 2 * h + 1),
+                                __shfl_sync(0xffffffffu, bia, 2 * h + 1));
+          o[h] = pack_bf16x2(v0, v1);
+        }
+        if (m < p.M && nb < p.N) {
+          uint4 *dst = reinterpret_cast<uint4 *>(yrow + nb);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (nb + 8 * g < p.N) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+    if (!ok) *abort_flag = 1;
   }
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, QLIN_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, BN);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ========================================== swap-AB GEMM with A in tensor memory
@@ -628,24 +672,20 @@ static cudaError_t set_smem(KernelT kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int BN>
-static cudaError_t launch_fp8_bn(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
-  using C = Fp8Cfg<BN>;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, g.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.M, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.N, g.K, C::BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  static cudaError_t attr = set_smem(k_fp8_gemm<BN>, C::SMEM);
-  if (attr != cudaSuccess) return attr;
-  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, g.w_scale, g.x_scale, g.bias, (uint16_t *)g.y, dev.status};
-  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + C::BM - 1) / C::BM));
-  return launch_kernel(k_fp8_gemm<BN>, grid, dim3(256), C::SMEM, st, 1, ta, tb, p);
-}
-
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
   if (g.M == 0) return cudaSuccess;
-  if (g.N % 256 == 0 || g.N > 1024) return launch_fp8_bn<256>(g, dev, st);
-  return launch_fp8_bn<128>(g, dev, st);
+  using C = Fp8Cfg;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, g.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.M, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.N, g.K, C::BK, C::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  static cudaError_t attr = set_smem(k_fp8_gemm, C::SMEM);
+  if (attr != cudaSuccess) return attr;
+  const int mtiles = (int)((g.M + C::BM - 1) / C::BM), ntiles = (int)((g.N + C::BN - 1) / C::BN);
+  const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
+  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.w_scale, g.x_scale, g.bias, (uint16_t *)g.y,
+              dev.status};
+  return launch_kernel(k_fp8_gemm, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, p);
 }
 
 int w8_swap_bnt(int64_t M) {

@@ -89,8 +89,7 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_W8A8_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
-      if (qtype == QLIN_E4M3) return (N % 256 == 0 || N > 1024) ? "k_quantize_act+k_fp8_gemm<256>"
-                                                                  : "k_quantize_act+k_fp8_gemm<128>";
+      if (qtype == QLIN_E4M3) return "k_quantize_act+k_fp8_gemm";
       static const char *names[3] = {"k_quantize_act_i8bf16+k_w8_dq<16,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<32,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<64,i8>"};
