@@ -163,8 +163,16 @@ class GpuWorkload:
         self.copies = copies if self.weight_bytes < 4 * L2_BYTES else 1
         self.wsets = [dict() for _ in range(self.copies)]
         self.scales = {}
+        # the 36-layer stack draws its tensors with a seeded device generator
+        # (same distributions; host generation of 2.8 G weights would take minutes)
+        self.device_gen = name.startswith("stack")
         for key, l in wkeys.items():
-            w = torch.from_numpy(synth.make_inputs(l, want=("w",))["w"]).to(dev)
+            if self.device_gen:
+                g = torch.Generator(device=dev)
+                g.manual_seed(synth.sub_seed(l.workload, l.layer, f"{l.name}.K{l.K}.N{l.N}", "weight") % (2 ** 63))
+                w = torch.randn((l.N, l.K), generator=g, device=dev, dtype=torch.float32) * (1.0 / l.K ** 0.5)
+            else:
+                w = torch.from_numpy(synth.make_inputs(l, want=("w",))["w"]).to(dev)
             qw, s = capi.quantize_weight(l.qtype, w)
             del w
             self.scales[key] = s
@@ -174,28 +182,54 @@ class GpuWorkload:
         # activations, calibration scales, bias, outputs
         self.x, self.y, self.bias, self.sx, self.ws = [], [], [], [], []
         self.x_host, self.y_host = [], []
-        cache = {}
+        cache, shared = {}, {}
+        def dev_normal(shape, role, l):
+            g = torch.Generator(device=dev)
+            g.manual_seed(synth.sub_seed(l.workload, l.layer, f"{l.name}.K{l.K}.M{l.M}", role) % (2 ** 63))
+            return torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
         for l in self.lins:
             k = (l.workload, l.layer, l.name, l.K, l.M)
-            if k not in cache:
-                t = synth.make_inputs(l, want=("x", "cal", "bias"))
-                cache[k] = t
-            t = cache[k]
-            xt = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+            if self.device_gen:
+                t = {"x_dev": dev_normal((l.M, l.K), "act", l)}
+                if l.form == "w8a8":
+                    t["cal_dev"] = dev_normal((synth.CALIB_ROWS, l.K), "calib", l)
+            else:
+                if k not in cache:
+                    cache[k] = synth.make_inputs(l, want=("x", "cal", "bias"))
+                t = cache[k]
+            shape_key = (l.form, l.qtype, l.M, l.K, l.N)
+            if self.device_gen:
+                # the stack's 216 calls are sequential on one stream: outputs, scratch and
+                # pinned host staging are shared per shape (each layer keeps its own x)
+                xt = t["x_dev"]
+                if ("xh",) + shape_key not in shared:
+                    shared[("xh",) + shape_key] = xt.cpu().pin_memory()
+                    shared[("y",) + shape_key] = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
+                    shared[("yh",) + shape_key] = torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory()
+                self.x_host.append(shared[("xh",) + shape_key])
+                self.y.append(shared[("y",) + shape_key])
+                self.y_host.append(shared[("yh",) + shape_key])
+            else:
+                xt = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+                self.x_host.append(torch.from_numpy(t["x"].view(np.int16)).view(torch.bfloat16).pin_memory())
+                self.y.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
+                self.y_host.append(torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory())
             self.x.append(xt)
-            self.x_host.append(torch.from_numpy(t["x"].view(np.int16)).view(torch.bfloat16).pin_memory())
-            self.y.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
-            self.y_host.append(torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory())
             self.bias.append(torch.from_numpy(t["bias"].view(np.int16)).to(dev).view(torch.bfloat16)
                              if "bias" in t else None)
             if l.form == "w8a8":
-                cal = torch.from_numpy(t["cal"].view(np.int16)).to(dev).view(torch.bfloat16)
+                cal = t["cal_dev"] if self.device_gen else \
+                    torch.from_numpy(t["cal"].view(np.int16)).to(dev).view(torch.bfloat16)
                 self.sx.append(capi.act_scale_from_calib(l.qtype, cal))
                 del cal
-                self.ws.append(capi.workspace(capi.QLIN_OP_W8A8_LINEAR, l.qtype, l.M, l.K, l.N, device=dev))
+                op = capi.QLIN_OP_W8A8_LINEAR
             else:
                 self.sx.append(None)
-                self.ws.append(capi.workspace(capi.QLIN_OP_W8A16_LINEAR, l.qtype, l.M, l.K, l.N, device=dev))
+                op = capi.QLIN_OP_W8A16_LINEAR
+            if ("ws",) + shape_key not in shared or not self.device_gen:
+                shared[("ws",) + shape_key] = capi.workspace(op, l.qtype, l.M, l.K, l.N, device=dev)
+            self.ws.append(shared[("ws",) + shape_key])
             if len(cache) > 8:
                 cache.clear()
         torch.cuda.synchronize()
@@ -357,6 +391,25 @@ def cpu_baseline(name, unit_scale, unit):
             "sample": desc + f"; {n} timed repetitions, {dt:.3f} s each"}
 
 
+# ------------------------------------------------------- replicas (N > 1)
+def max_over_ranks(value: float, device) -> float:
+    """Largest `value` over all ranks (the job's wall time is its slowest
+    replica's); identity without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_step: float, steps: int, world: int, elapsed_max: float, unit_scale: float) -> float:
+    """Weak scaling: every replica processes the same per-step units; the job
+    processed world x steps x units in the slowest replica's time."""
+    return units_per_step * steps * world / elapsed_max / unit_scale
+
+
 # ------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -451,14 +504,10 @@ def main():
         barrier()
     # graph replays do not pass through the host entry points: count the kernels a step launches
     launches = sum(len(k.split("+")) for k in W.kernel) * a.steps
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, dev)
     clocks = clk.summary()
     ms_step = elapsed / a.steps * 1e3
-    value = units_step * a.steps * world / elapsed / unit_scale
+    value = whole_job_value(units_step, a.steps, world, elapsed, unit_scale)
 
     # ---- timed region 2: per-launch durations (each call bracketed by CUDA events) ----
     dur = np.zeros((a.steps, n))
@@ -530,12 +579,8 @@ def main():
             W.graphs_e2e[s % W.copies].replay()
         e1.record(W.stream)
         torch.cuda.synchronize()
-        et = e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            t = torch.tensor([et], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            et = float(t.item())
-        e2e = {"value": units_step * a.steps * world / et / unit_scale, "unit": metric_unit,
+        et = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+        e2e = {"value": whole_job_value(units_step, a.steps, world, et, unit_scale), "unit": metric_unit,
                "h2d_bytes_per_step": int(sum(2 * l.M * l.K for l in W.lins)),
                "d2h_bytes_per_step": int(sum(2 * l.M * l.N for l in W.lins)),
                "how": "CUDA-graph replay: pinned-host activations copied in, the linears, outputs copied out"}
