@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         mma_commit(&acc_full[b]);
       }
+      // Drain: no commit arrival may still be in flight towards this CTA's shared
+      // memory when it exits (a successor CTA on this SM may already own it).
+      if (i > 0) ok = mbar_wait(&empty[(i - 1) % C::STAGES], ((i - 1) / C::STAGES) & 1, abort_flag) && ok;
       if (!ok) *abort_flag = 1;
     }
   } else if (warp >= 4) {  // ------------------------- epilogue
@@ -458,7 +461,8 @@ __global__ void __launch_bounds__(640, 1)
     if (lane == 0) {
       const int e = warp == 1 ? 0 : 1;
       bool ok = true;
-      int cidx = 0;  // chunk counter (same sequence as the epilogue's)
+      int cidx = 0;    // chunk counter (same sequence as the epilogue's)
+      int last = -1;   // this issuer's last block
       for (int j = 0; j < my_units && ok; ++j) {
         for (int cb = 0; cb < nkb && ok; cb += CH, ++cidx) {  // chunk = k-blocks [cb, ce)
           const int ce = min(nkb, cb + CH);
@@ -488,10 +492,17 @@ __global__ void __launch_bounds__(640, 1)
             mma_bf16_ts(dt, at + 24, bd + 6, C::IDESC, 1u);
             mma_commit(&x_empty[sx]);
             mma_commit(&a_empty[sa]);
+            last = i;
           }
           if (!ok) break;
           mma_commit(&acc_full[db]);  // arrives when this issuer's MMAs of the chunk are done
         }
+      }
+      // Drain: the CTA must not exit with a commit arrival still in flight towards
+      // its shared memory (a successor CTA on this SM may already own it).
+      if (last >= 0) {
+        ok = mbar_wait(&x_empty[last % C::X], (last / C::X) & 1, abort_flag) &&
+             mbar_wait(&a_empty[last % C::NA], (last / C::NA) & 1, abort_flag) && ok;
       }
       if (!ok) *abort_flag = 1;
     }
