@@ -282,25 +282,38 @@ struct DqCfg {
   static constexpr int BM = 128, BK = 64;
   static constexpr int RAW_BYTES = BM * BK;     // 8-bit weight tile, 64-byte swizzle
   static constexpr int X_BYTES = BNT * BK * 2;  // BF16 activation tile, 128-byte swizzle
-  static constexpr int X = BNT <= 64 ? (65536 / X_BYTES > 16 ? 16 : 65536 / X_BYTES) : (BNT == 128 ? 6 : 3);
-  static constexpr int RING = 200 * 1024;
-  static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
-  static constexpr int R = R0 > 16 ? 16 : R0;
-  static constexpr int X_OFF = 0, RAW_OFF = X * X_BYTES, BAR_OFF = RAW_OFF + R * RAW_BYTES;
-  static constexpr int SMEM = BAR_OFF + 1024 + 1024;  // alignment slack + barriers
+  static constexpr int QUADS = 3;               // converter warp quads
+  static constexpr int THREADS = 640;           // 20 warps
   // Accumulators.  A chain of MMAs into one small tile is bound by the MMA's
   // accumulate latency, not its throughput, so consecutive k-blocks rotate
   // over NACC independent accumulator tiles (summed in a fixed order by the
   // epilogue); ND sets of them alternate between consecutive output tiles.
   static constexpr int NACC = BNT <= 32 ? 4 : BNT <= 128 ? 2 : 1;
-  static constexpr int DSTRIDE = NACC * BNT;                // columns of one accumulator set
+  static constexpr int ISSUERS = NACC >= 2 ? 2 : 1;  // MMA-issuing threads (own accumulators each)
+  static constexpr int DSTRIDE = NACC * BNT;         // columns of one accumulator set
   static constexpr int ND = 2 * DSTRIDE <= 256 ? 2 : 1;
   static constexpr int ACOL = ND * DSTRIDE <= 128 ? 128 : 256;  // first TMEM column of the A ring
-  static constexpr int NA = (512 - ACOL) / 32 > 12 ? 12 : (512 - ACOL) / 32;  // A stages, 32 columns each
-  static constexpr int QUADS = 3;                           // converter warp quads
-  static constexpr int ISSUERS = NACC >= 2 ? 2 : 1;         // MMA-issuing threads (own accumulators each)
-  static constexpr int THREADS = 640;                       // 20 warps
+  // Ring depths.  mbarrier.try_wait.parity only tells the current phase from
+  // the previous one, so a waiter must never be more than one phase ahead of a
+  // slot.  Every waiter below is one of several consumers that take blocks
+  // round-robin; it is safe when the previous use of its slot was its own
+  // earlier block, i.e. when the ring depth is a multiple of the number of
+  // consumers sharing that ring:
+  //   raw ring      (3 converter quads)               R  % 3 == 0
+  //   TMEM A ring   (3 quads wait a_empty, issuers     NA % 6 == 0
+  //                  wait a_full)
+  //   activations   (ISSUERS MMA threads)             X  % ISSUERS == 0
+  static constexpr int NA = ACOL == 128 ? 12 : 6;  // A stages, 32 columns (64 BF16 k) each
+  static constexpr int X = BNT <= 32 ? 16 : BNT == 64 ? 8 : BNT == 128 ? 8 : 4;
+  static constexpr int RING = 200 * 1024;
+  static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
+  static constexpr int R = (R0 > 15 ? 15 : R0) / 3 * 3;  // raw stages
+  static constexpr int X_OFF = 0, RAW_OFF = X * X_BYTES, BAR_OFF = RAW_OFF + R * RAW_BYTES;
+  static constexpr int SMEM = BAR_OFF + 1024 + 1024;  // alignment slack + barriers
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
+  static_assert(R % QUADS == 0 && R >= 6, "raw ring depth: multiple of the converter quads");
+  static_assert(NA % (QUADS * ISSUERS) == 0, "A ring depth: multiple of quads x issuers");
+  static_assert(X % ISSUERS == 0, "activation ring depth: multiple of the MMA issuers");
   static_assert(ND * DSTRIDE <= ACOL && ACOL + NA * 32 <= 512, "TMEM columns");
   static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
