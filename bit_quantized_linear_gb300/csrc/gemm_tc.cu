@@ -404,27 +404,30 @@ __global__ void __launch_bounds__(640, 1)
   const int total = my_units * nkb;
   const int chunks_per_unit = (nkb + CH - 1) / CH;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::R; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);  // the four warps of the quad that read the tile
+  {  // barrier initialisation spread over the threads (one barrier each)
+    const int t = threadIdx.x;
+    constexpr int B0 = C::R, B1 = 2 * C::R, B2 = B1 + C::X, B3 = B2 + C::X, B4 = B3 + C::NA, B5 = B4 + C::NA,
+                  B6 = B5 + C::ND, B7 = B6 + C::ND;
+    static_assert(B7 < C::THREADS, "one thread per barrier");
+    uint64_t *bar = nullptr;
+    uint32_t cnt = 1;
+    if (t < B0) bar = &raw_full[t];
+    else if (t < B1) bar = &raw_empty[t - B0], cnt = 4;  // the four warps of the quad that read it
+    else if (t < B2) bar = &x_full[t - B1];
+    else if (t < B3) bar = &x_empty[t - B2];
+    else if (t < B4) bar = &a_full[t - B3], cnt = 4;     // the converter quad
+    else if (t < B5) bar = &a_empty[t - B4];
+    else if (t < B6) bar = &acc_full[t - B5], cnt = C::ISSUERS;  // one commit per MMA issuer
+    else if (t < B7) bar = &acc_empty[t - B6], cnt = 4;          // the epilogue quad
+    if (bar) {
+      mbar_init(bar, cnt);
+      fence_barrier_init();
     }
-    for (int s = 0; s < C::X; ++s) {
-      mbar_init(&x_full[s], 1);
-      mbar_init(&x_empty[s], 1);
+    if (t == C::THREADS - 1) {
+      *abort_flag = 0;
+      tma_prefetch_desc(&tm_w);
+      tma_prefetch_desc(&tm_x);
     }
-    for (int s = 0; s < C::NA; ++s) {
-      mbar_init(&a_full[s], 4);
-      mbar_init(&a_empty[s], 1);
-    }
-    for (int s = 0; s < C::ND; ++s) {
-      mbar_init(&acc_full[s], C::ISSUERS);  // one commit per MMA issuer
-      mbar_init(&acc_empty[s], 4);          // the epilogue quad
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-    tma_prefetch_desc(&tm_w);
-    tma_prefetch_desc(&tm_x);
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();

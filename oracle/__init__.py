@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
             L.orc_w8a8.restype = None
             L.orc_w8a16.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, P]
             L.orc_w8a16.restype = None
+            L.orc_quantize_act_per_token.argtypes = [I, I64, I64, P, P, P]
+            L.orc_quantize_act_per_token.restype = None
+            L.orc_w8a8_per_token.argtypes = [I, I64, I64, I64, P, P, P, P, P, P, I64, P]
+            L.orc_w8a8_per_token.restype = None
             L.orc_num_threads.argtypes = []
             L.orc_num_threads.restype = I
             _lib = L
@@ -160,6 +164,32 @@ def w8a16(qtype: int, x_bf16, qw, s_w, bias=None, rows=None) -> np.ndarray:
     r, R = _rows(rows, M)
     y = np.empty((R, N), np.float64)
     lib().orc_w8a16(qtype, M, K, N, _ptr(x), _ptr(qw), _ptr(s_w), _ptr(b), _ptr(r), R, _ptr(y))
+    return y
+
+
+def quantize_act_per_token(qtype: int, x_bf16):
+    """Dynamic per-token quantization: (q uint8 [M,K], s_x float32 [M])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((M,), np.float32)
+    lib().orc_quantize_act_per_token(qtype, M, K, _ptr(x), _ptr(s), _ptr(q))
+    return q, s
+
+
+def w8a8_per_token(qtype: int, qx, s_x, qw, s_w, bias=None, rows=None) -> np.ndarray:
+    """fp64 W8A8 reference with one activation scale per token row."""
+    qx = _c(qx, np.uint8)
+    qw = _c(qw, np.uint8)
+    s_x = _c(s_x, np.float32)
+    s_w = _c(s_w, np.float32)
+    M, K = qx.shape
+    N = qw.shape[0]
+    b = None if bias is None else _c(bias, np.uint16)
+    r, R = _rows(rows, M)
+    y = np.empty((R, N), np.float64)
+    lib().orc_w8a8_per_token(qtype, M, K, N, _ptr(qx), _ptr(s_x), _ptr(qw), _ptr(s_w), _ptr(b), _ptr(r), R,
+                             _ptr(y))
     return y
 
 

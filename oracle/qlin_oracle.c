@@ -218,6 +218,54 @@ void orc_w8a16(int qtype, int64_t M, int64_t K, int64_t N, const uint16_t *x,
     }
 }
 
+/* ---- dynamic per-token activation quantization -------------------------
+ * The contrast the "Nano-vLLM-MOE" README draws for W8A8 static ("INT8 量化支持",
+ * 关键设计, W8A8 static item): a dynamic per-token abs-max costs one more
+ * reduction than the static scalar.  Per token row m:
+ *   s_x[m] = fl32(max_k |x[m,k]| / QMAX)   (1 for an all-zero row)
+ *   q[m,k] = Q(fl32(x[m,k] / s_x[m])). */
+void orc_quantize_act_per_token(int qtype, int64_t M, int64_t K, const uint16_t *x, float *s_x,
+                                uint8_t *q) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      float a = fabsf(bf16_to_f32(x[m * K + k]));
+      if (a > amax) amax = a;
+    }
+    const float s = (amax > 0.0f) ? amax / qmax_of(qtype) : 1.0f;
+    s_x[m] = s;
+    for (int64_t k = 0; k < K; ++k) q[m * K + k] = quantize_value(qtype, bf16_to_f32(x[m * K + k]), s);
+  }
+}
+
+/* W8A8 with one activation scale per token row:
+ *   y[m,n] = acc[m,n] * s_x[m] * s_w[n] + bias[n]   (acc as in orc_w8a8). */
+void orc_w8a8_per_token(int qtype, int64_t M, int64_t K, int64_t N, const uint8_t *qx, const float *s_x,
+                        const uint8_t *qw, const float *s_w, const uint16_t *bias, const int64_t *rows,
+                        int64_t nrows, double *y) {
+  int64_t R = rows ? nrows : M;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t i = 0; i < R; ++i)
+    for (int64_t n = 0; n < N; ++n) {
+      int64_t m = pick_row(rows, i);
+      double acc;
+      if (qtype == ORC_INT8) {
+        int64_t a = 0;
+        for (int64_t k = 0; k < K; ++k)
+          a += (int64_t)(int8_t)qx[m * K + k] * (int64_t)(int8_t)qw[n * K + k];
+        acc = (double)a;
+      } else {
+        acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+          acc += orc_e4m3_decode(qx[m * K + k]) * orc_e4m3_decode(qw[n * K + k]);
+      }
+      double v = acc * (double)s_x[m] * (double)s_w[n];
+      if (bias) v += (double)bf16_to_f32(bias[n]);
+      y[i * N + n] = v;
+    }
+}
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int orc_num_threads(void) {
 #ifdef _OPENMP

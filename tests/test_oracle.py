@@ -455,3 +455,65 @@ def test_quantizers_use_ieee_division(orc):
         c_div, c_rcp = code(v_div), code(v_rcp)
         assert (c_div != c_rcp).sum() >= 10, "no discriminating element in the sample"
         assert np.array_equal(q, c_div)
+
+
+# ------------------------------------------- dynamic per-token activations
+@pytest.mark.parametrize("qt", [INT8, E4M3])
+def test_per_token_scales_and_extremes(orc, qt):
+    rng = np.random.default_rng(61)
+    x = synth.activations(9, 96, rng, synth.outlier_channels(96, rng))
+    xf = synth.bf16_bits_to_f32(x)
+    xf[3] = 0.0
+    x = synth.f32_to_bf16_bits(xf)
+    q, s = orc.quantize_act_per_token(qt, x)
+    qmax = np.float32(127 if qt == INT8 else 448)
+    for m in range(9):
+        amax = np.abs(xf[m]).max()
+        assert s[m] == (amax / qmax if amax > 0 else np.float32(1.0))
+        if amax > 0:
+            j = np.abs(xf[m]).argmax()
+            code = q[m, j]
+            assert (abs(int(code.view(np.int8))) == 127) if qt == INT8 else ((code & 0x7F) == 0x7E)
+    assert np.all(q[3] == 0) and s[3] == 1.0
+
+
+@pytest.mark.parametrize("qt", [INT8, E4M3])
+def test_per_token_equals_static_when_rows_share_amax(orc, qt):
+    """Rows with the same abs-max: the per-token quantizer reduces to the static
+    one with that abs-max as calibration maximum."""
+    rng = np.random.default_rng(62)
+    xf = rng.standard_normal((7, 64)).astype(np.float32)
+    xf[:, 5] = 6.0  # every row's largest magnitude
+    x = synth.f32_to_bf16_bits(xf)
+    q, s = orc.quantize_act_per_token(qt, x)
+    s_static = orc.act_scale(qt, x)
+    assert np.all(s == s_static)
+    assert np.array_equal(q, orc.quantize_act(qt, x, s_static))
+
+
+@pytest.mark.parametrize("qt", [INT8, E4M3])
+def test_per_token_row_scaling_and_reference(orc, qt):
+    """Scaling one token row by 2^j changes only that row's scale (by 2^j) and
+    leaves every code and the W8A8 output of the other rows unchanged; the row's
+    own output scales exactly.  The reference matches exact rationals."""
+    rng = np.random.default_rng(63)
+    M, K, N = 5, 48, 6
+    xf = synth.bf16_bits_to_f32(synth.activations(M, K, rng))
+    q1, s1 = orc.quantize_act_per_token(qt, synth.f32_to_bf16_bits(xf))
+    xf2 = xf.copy()
+    xf2[2] *= np.float32(8)
+    q2, s2 = orc.quantize_act_per_token(qt, synth.f32_to_bf16_bits(xf2))
+    assert np.array_equal(q1, q2)
+    assert s2[2] == s1[2] * 8 and np.array_equal(np.delete(s1, 2), np.delete(s2, 2))
+    qw, sw = orc.quantize_weight(qt, synth.weights(N, K, rng))
+    b = synth.bias(N, rng)
+    y1 = orc.w8a8_per_token(qt, q1, s1, qw, sw, b)
+    y2 = orc.w8a8_per_token(qt, q2, s2, qw, sw)
+    y1nb = orc.w8a8_per_token(qt, q1, s1, qw, sw)
+    assert np.array_equal(y2[2], 8 * y1nb[2]) and np.array_equal(np.delete(y2, 2, 0), np.delete(y1nb, 2, 0))
+    bf = synth.bf16_bits_to_f32(b)
+    for m in range(M):
+        for n in range(N):
+            acc = sum(_exact_deq(qt, q1[m, k], orc) * _exact_deq(qt, qw[n, k], orc) for k in range(K))
+            ref = acc * Fraction(float(s1[m])) * Fraction(float(sw[n])) + Fraction(float(bf[n]))
+            assert abs(Fraction(y1[m, n]) - ref) <= abs(ref) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 80)
