@@ -54,6 +54,8 @@ def workload_calls(name: str):
         return synth.workload(synth.W8A8_3B).linears, synth.W8A8_3B
     if name == "prefill":
         return synth.workload(synth.PREFILL).linears, synth.PREFILL
+    if name == "w8a8-dyn-3b":
+        return synth.workload(synth.W8A8_DYN_3B).linears, synth.W8A8_DYN_3B
     if name == "stack-decode":
         return synth.stack_linears("decode"), synth.STACK + "-decode"
     if name == "stack-prefill":
@@ -218,7 +220,10 @@ class GpuWorkload:
             self.x.append(xt)
             self.bias.append(torch.from_numpy(t["bias"].view(np.int16)).to(dev).view(torch.bfloat16)
                              if "bias" in t else None)
-            if l.form == "w8a8":
+            if l.form == "w8a8dyn":
+                self.sx.append(None)
+                op = capi.QLIN_OP_W8A8_DYNAMIC_LINEAR
+            elif l.form == "w8a8":
                 cal = t["cal_dev"] if self.device_gen else \
                     torch.from_numpy(t["cal"].view(np.int16)).to(dev).view(torch.bfloat16)
                 self.sx.append(capi.act_scale_from_calib(l.qtype, cal))
@@ -245,7 +250,12 @@ class GpuWorkload:
             qt = capi.QTYPES[l.qtype]
             ws = self.ws[i]
             wsp, wsb = (None, 0) if ws is None else (ptr(ws), ws.numel())
-            if l.form == "w8a16":
+            if l.form == "w8a8dyn":
+                self.fns.append(L.qlin_w8a8_dynamic_linear)
+                for c in range(self.copies):
+                    self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.wsets[c][key]),
+                                         ptr(self.scales[key]), ptr(self.bias[i]), ptr(self.y[i]), wsp, wsb, sp))
+            elif l.form == "w8a16":
                 self.fns.append(L.qlin_w8a16_linear)
                 for c in range(self.copies):
                     self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.wsets[c][key]),
@@ -256,7 +266,8 @@ class GpuWorkload:
                     self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.sx[i]),
                                          ptr(self.wsets[c][key]), ptr(self.scales[key]), ptr(self.bias[i]),
                                          ptr(self.y[i]), wsp, wsb, sp))
-        op = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR}
+        op = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR,
+              "w8a8dyn": capi.QLIN_OP_W8A8_DYNAMIC_LINEAR}
         self.kernel = [capi.qlin_kernel_name(op[l.form], l.qtype, l.M, l.K, l.N) for l in self.lins]
 
     def _capture(self, copy, events=None, e2e=False):
@@ -358,7 +369,7 @@ def oracle_sample(name, rows_per_call=1):
         r = min(l.M, rows_per_call)
         # the first r rows of the workload's activations (the generator draws rows in order)
         x = synth.make_inputs(l, want=("x",), x_rows=r)["x"]
-        sx = oracle.act_scale(qt, t["cal"]) if l.form == "w8a8" else None
+        sx = oracle.act_scale(qt, t["cal"]) if l.form == "w8a8" and "cal" in t else None
         sub = synth.Linear(l.name, l.K, l.N, r, l.qtype, l.form, l.bias, l.outliers, l.workload, l.layer)
         prepared.append((l, sub, qt, q, s, x, sx, t.get("bias")))
 
@@ -366,6 +377,9 @@ def oracle_sample(name, rows_per_call=1):
         for l, sub, qt, q, s, x, sx, b in prepared:
             if l.form == "w8a16":
                 oracle.w8a16(qt, x, q, s, b)
+            elif l.form == "w8a8dyn":
+                qx, sxr = oracle.quantize_act_per_token(qt, x)
+                oracle.w8a8_per_token(qt, qx, sxr, q, s, b)
             else:
                 qx = oracle.quantize_act(qt, x, sx)
                 oracle.w8a8(qt, qx, sx, q, s, b)
@@ -418,7 +432,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     ap.add_argument("--workload", default="decode7b",
-                    choices=["decode7b", "small", "w8a8-3b", "prefill", "stack-decode", "stack-prefill"])
+                    choices=["decode7b", "small", "w8a8-3b", "w8a8-dyn-3b", "prefill", "stack-decode",
+                             "stack-prefill"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()

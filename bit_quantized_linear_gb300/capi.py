@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libqlin.so")
 QLIN_OK, QLIN_ERR_INVALID_ARG, QLIN_ERR_UNSUPPORTED, QLIN_ERR_WORKSPACE, QLIN_ERR_CUDA, QLIN_ERR_TIMEOUT = range(6)
 QLIN_INT8, QLIN_E4M3 = 0, 1
 (QLIN_OP_QUANTIZE_WEIGHT, QLIN_OP_ACT_SCALE, QLIN_OP_QUANTIZE_ACT, QLIN_OP_W8A16_LINEAR,
- QLIN_OP_W8A8_LINEAR, QLIN_OP_I8_GEMM_S32) = range(6)
+ QLIN_OP_W8A8_LINEAR, QLIN_OP_I8_GEMM_S32, QLIN_OP_W8A8_DYNAMIC_LINEAR) = range(7)
 
 QTYPES = {"int8": QLIN_INT8, "e4m3": QLIN_E4M3}
 
@@ -27,7 +27,8 @@ QTYPES = {"int8": QLIN_INT8, "e4m3": QLIN_E4M3}
 EXPORTS = ["qlin_quantize_weight", "qlin_act_scale_from_calib", "qlin_quantize_act_static",
            "qlin_w8a16_linear", "qlin_w8a8_linear", "qlin_i8_gemm_s32", "qlin_workspace_bytes",
            "qlin_get_device_status", "qlin_status_string", "qlin_version", "qlin_debug_wait_flag",
-           "qlin_kernel_name", "qlin_launch_count", "qlin_w8a8_linear_noalloc"]
+           "qlin_kernel_name", "qlin_launch_count", "qlin_w8a8_linear_noalloc",
+           "qlin_quantize_act_dynamic", "qlin_w8a8_dynamic_linear"]
 
 # Size of the library-owned scratch of qlin_w8a8_linear_noalloc (QLIN_W8A8_NOALLOC_SCRATCH_BYTES).
 W8A8_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -59,6 +60,8 @@ def _load() -> ctypes.CDLL:
         "qlin_kernel_name": [I, I, I64, I64, I64],
         "qlin_launch_count": [],
         "qlin_w8a8_linear_noalloc": [I, I64, I64, I64, P, P, P, P, P, P, P],
+        "qlin_quantize_act_dynamic": [I, I64, I64, P, P, P, P],
+        "qlin_w8a8_dynamic_linear": [I, I64, I64, I64, P, P, P, P, P, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -153,6 +156,20 @@ def qlin_w8a8_linear_noalloc(qtype, x, input_scale, qw, w_scale, bias, y, stream
                                          _p(bias), _p(y), _stream(stream)), "qlin_w8a8_linear_noalloc")
 
 
+def qlin_quantize_act_dynamic(qtype, x, qx, x_scale, stream=None):
+    M, K = x.shape
+    _check(_lib.qlin_quantize_act_dynamic(_qt(qtype), M, K, _p(x), _p(qx), _p(x_scale), _stream(stream)),
+           "qlin_quantize_act_dynamic")
+
+
+def qlin_w8a8_dynamic_linear(qtype, x, qw, w_scale, bias, y, ws, stream=None):
+    M, K = x.shape
+    N = qw.shape[0]
+    wp, wb = _ws(ws)
+    _check(_lib.qlin_w8a8_dynamic_linear(_qt(qtype), M, K, N, _p(x), _p(qw), _p(w_scale), _p(bias), _p(y),
+                                         wp, wb, _stream(stream)), "qlin_w8a8_dynamic_linear")
+
+
 def qlin_i8_gemm_s32(qx, qw, acc, ws=None, stream=None):
     M, K = qx.shape
     N = qw.shape[0]
@@ -224,6 +241,22 @@ def w8a8_linear(qtype, x, input_scale, qw, w_scale, bias=None):
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     ws = workspace(QLIN_OP_W8A8_LINEAR, qtype, M, K, N, device=x.device)
     qlin_w8a8_linear(qtype, x, input_scale, qw, w_scale, bias, y, ws)
+    return y
+
+
+def quantize_act_dynamic(qtype, x):
+    qx = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    s = torch.empty((x.shape[0],), dtype=torch.float32, device=x.device)
+    qlin_quantize_act_dynamic(qtype, x, qx, s)
+    return qx, s
+
+
+def w8a8_dynamic_linear(qtype, x, qw, w_scale, bias=None):
+    M, K = x.shape
+    N = qw.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws = workspace(QLIN_OP_W8A8_DYNAMIC_LINEAR, qtype, M, K, N, device=x.device)
+    qlin_w8a8_dynamic_linear(qtype, x, qw, w_scale, bias, y, ws)
     return y
 
 

@@ -83,6 +83,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 struct Fp8Params {
   int M, N, K;
   int mtiles, ntiles;
+  int xs_per_token;  // x_scale holds one scale per token row
   const float *w_scale;
   const float *x_scale;
   const uint16_t *bias;
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp >= 4) {  // ------------------------- epilogue
     const int q4 = warp & 3, half = (warp - 4) >> 2;  // half h owns channels [128h, 128h + 128)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const float sx = __ldg(p.x_scale);
+    const float sx = p.xs_per_token ? 1.0f : __ldg(p.x_scale);
     bool ok = true;
     for (int j = 0; j < my_tiles && ok; ++j) {
       const int t = blockIdx.x + j * G, b = j & 1;
@@ -208,6 +209,8 @@ __global__ void __launch_bounds__(384, 1)
       }
       const int m = m0 + q4 * 32 + lane;
       uint16_t *yrow = p.y + (size_t)m * p.N;
+      // per-token activation scale multiplies the row (lane = token)
+      const float sxm = p.xs_per_token ? (m < p.M ? __ldg(p.x_scale + m) : 0.0f) : 1.0f;
 #pragma unroll 1
       for (int c = 128 * half; c < 128 * half + 128; c += 32) {
         uint32_t r[32];
@@ -221,9 +224,9 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t o[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float v0 = fmaf(__uint_as_float(r[2 * h]), __shfl_sync(0xffffffffu, scl, 2 * h),
+          const float v0 = fmaf(__uint_as_float(r[2 * h]), sxm * __shfl_sync(0xffffffffu, scl, 2 * h),
                                 __shfl_sync(0xffffffffu, bia, 2 * h));
-          const float v1 = fmaf(__uint_as_float(r[2 * h + 1]), __shfl_sync(0xffffffffu, scl, 2 * h + 1),
+          const float v1 = fmaf(__uint_as_float(r[2 * h + 1]), sxm * __shfl_sync(0xffffffffu, scl, 2 * h + 1),
                                 __shfl_sync(0xffffffffu, bia, 2 * h + 1));
           o[h] = pack_bf16x2(v0, v1);
         }
@@ -267,7 +270,8 @@ enum SwapMode { kSwapW8A16 = 0, kSwapI8Scaled = 1, kSwapI8Raw = 2 };
 
 struct SwapParams {
   int M, N, K;
-  int splits;  // CTAs per cluster along K (gridDim.z)
+  int xs_per_token;  // x_scale holds one scale per token (I8 scaled mode)
+  int splits;        // CTAs per cluster along K (gridDim.z)
   int units;   // output tiles: n-tiles x token tiles
   int ntiles;  // n-tiles (128 channels each)
   const float *w_scale;
@@ -359,7 +363,7 @@ __device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const 
   if constexpr (MODE == kSwapI8Raw) {
     *reinterpret_cast<uint4 *>((int32_t *)p.y + (size_t)m * p.N + n) = make_uint4(v[0], v[1], v[2], v[3]);
   } else {
-    const float sx = MODE == kSwapI8Scaled ? __ldg(p.x_scale) : 1.0f;
+    const float sx = MODE == kSwapI8Scaled ? __ldg(p.x_scale + (p.xs_per_token ? m : 0)) : 1.0f;
     uint32_t o[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -643,12 +647,15 @@ __global__ void __launch_bounds__(640, 1)
                 for (int c = 0; c < BNT; ++c)
                   if (m0 + c < p.M) ((int32_t *)p.y)[(size_t)(m0 + c) * p.N + n] = sums[c];
               } else {
-                const float sc = __ldg(p.x_scale) * __ldg(p.w_scale + n);
+                const float sw = __ldg(p.w_scale + n);
+                const float sx0 = __ldg(p.x_scale);
                 const float b = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
 #pragma unroll
                 for (int c = 0; c < BNT; ++c)
-                  if (m0 + c < p.M)
+                  if (m0 + c < p.M) {
+                    const float sc = (p.xs_per_token ? __ldg(p.x_scale + m0 + c) : sx0) * sw;
                     ((uint16_t *)p.y)[(size_t)(m0 + c) * p.N + n] = f32_to_bf16_bits(fmaf((float)sums[c], sc, b));
+                  }
               }
             }
           } else {
@@ -710,8 +717,8 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   if (attr != cudaSuccess) return attr;
   const int mtiles = (int)((g.M + C::BM - 1) / C::BM), ntiles = (int)((g.N + C::BN - 1) / C::BN);
   const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.w_scale, g.x_scale, g.bias, (uint16_t *)g.y,
-              dev.status};
+  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.w_scale, g.x_scale, g.bias,
+              (uint16_t *)g.y, dev.status};
   return launch_kernel(k_fp8_gemm, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, p);
 }
 
@@ -744,7 +751,8 @@ static cudaError_t launch_dq_t(const GemmArgs &g, const void *xb, const DeviceIn
   const int units = ntiles * (int)((g.M + BNT - 1) / BNT);
   const int S = w8_swap_splits(units, g.K, dev.sms);
   const int G = S > 1 ? units : (units < dev.sms ? units : dev.sms);
-  SwapParams p{(int)g.M, (int)g.N, (int)g.K, S, units, ntiles, g.w_scale, g.x_scale, g.bias, g.y, dev.status};
+  SwapParams p{(int)g.M, (int)g.N,  (int)g.K, g.x_scale_per_token, S, units, ntiles, g.w_scale, g.x_scale,
+               g.bias,     g.y,        dev.status};
   return launch_kernel(k_w8_dq<BNT, QT, MODE>, dim3((unsigned)G, 1, (unsigned)S), dim3(C::THREADS), C::SMEM, st,
                        (unsigned)S, tw, tx, p);
 }

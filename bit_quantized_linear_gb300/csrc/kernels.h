@@ -68,9 +68,10 @@ struct GemmArgs {
   const void *a;          // x (BF16) or qx (codes)
   const void *qw;         // [N,K] codes
   const float *w_scale;   // [N]
-  const float *x_scale;   // device scalar (kW8A8) or null
+  const float *x_scale;   // device scalar (kW8A8), per-token [M] (x_scale_per_token), or null
   const uint16_t *bias;   // [N] or null
   void *y;                // [M,N] BF16, or int32 for kI8Raw
+  int x_scale_per_token = 0;  // x_scale holds one scale per token row (dynamic W8A8)
 };
 
 cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
@@ -87,6 +88,9 @@ int w8_swap_splits(int64_t tiles, int64_t K, int sms);
 cudaError_t launch_quantize_act_i8bf16(int64_t M, int64_t K, const void *x, const float *s, void *out, int sms,
                                        cudaStream_t st);
 cudaError_t launch_i8_to_bf16(int64_t M, int64_t K, const void *q, void *out, int sms, cudaStream_t st);
+// Dynamic per-token quantization: scales s[M]; codes (1 byte) or INT8 codes as BF16.
+cudaError_t launch_quantize_act_dyn(int qtype, bool out_bf16, int64_t M, int64_t K, const void *x, float *s, void *q,
+                                    cudaStream_t st);
 
 cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
                               cudaStream_t st);

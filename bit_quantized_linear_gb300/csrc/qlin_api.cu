@@ -86,6 +86,15 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
       const int b = i8_swap_bnt(M);
       return names[b == 16 ? 0 : b == 32 ? 1 : 2];
     }
+    case QLIN_OP_W8A8_DYNAMIC_LINEAR: {
+      if (check_linear_shape(M, K, N)) return "invalid";
+      if (M == 0) return "none";
+      if (qtype == QLIN_E4M3) return "k_quantize_act_dyn+k_fp8_gemm";
+      static const char *names[3] = {"k_quantize_act_dyn+k_w8_dq<16,i8>", "k_quantize_act_dyn+k_w8_dq<32,i8>",
+                                     "k_quantize_act_dyn+k_w8_dq<64,i8>"};
+      const int b = i8_swap_bnt(M);
+      return names[b == 16 ? 0 : b == 32 ? 1 : 2];
+    }
     case QLIN_OP_W8A8_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
@@ -122,6 +131,9 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     // quantized activations: E4M3 codes (1 byte), or INT8 codes as integer-valued BF16 (2 bytes)
     case QLIN_OP_W8A8_LINEAR: return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256);
     case QLIN_OP_I8_GEMM_S32: return round_up((size_t)M * (size_t)K * 2, 256);
+    // per-token codes (as for the static path) followed by the per-token scales
+    case QLIN_OP_W8A8_DYNAMIC_LINEAR:
+      return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256) + round_up((size_t)M * 4, 256);
   }
   return (size_t)-1;
 }
@@ -201,6 +213,40 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
   }
   if (launch_quantize_act_i8bf16(M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
   return from_cuda(launch_i8_swap(g, ws, false, *dev, st));
+}
+
+qlin_status qlin_quantize_act_dynamic(qlin_qtype qtype, int64_t M, int64_t K, const void *x, void *qx,
+                                      float *x_scale, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (M < 0 || K < 16 || (K % 16) || M > ((int64_t)1 << 31) - 1) return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !qx || !x_scale || !al16(x) || !al16(qx) || !al16(x_scale))) return QLIN_ERR_INVALID_ARG;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  return from_cuda(launch_quantize_act_dyn(qtype, false, M, K, x, x_scale, qx, (cudaStream_t)stream));
+}
+
+qlin_status qlin_w8a8_dynamic_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                                     const void *qw, const float *w_scale, const void *bias, void *y, void *ws,
+                                     size_t ws_bytes, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = check_linear_shape(M, K, N)) return s;
+  if (!qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias))) return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
+  const size_t need = qlin_workspace_bytes(QLIN_OP_W8A8_DYNAMIC_LINEAR, qtype, M, K, N);
+  if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool i8 = qtype == QLIN_INT8;
+  void *codes = ws;
+  float *scales = (float *)((char *)ws + round_up((size_t)M * (size_t)K * (i8 ? 2 : 1), 256));
+  if (launch_quantize_act_dyn(qtype, i8, M, K, x, scales, codes, st) != cudaSuccess) return QLIN_ERR_CUDA;
+  GemmArgs g{kW8A8, qtype, M, K, N, codes, qw, w_scale, scales, (const uint16_t *)bias, y};
+  g.x_scale_per_token = 1;
+  if (!i8) return from_cuda(launch_fp8_gemm(g, *dev, st));
+  return from_cuda(launch_i8_swap(g, codes, false, *dev, st));
 }
 
 qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, const void *qw,

@@ -162,6 +162,66 @@ __global__ void __launch_bounds__(256) k_i8_to_bf16(const uint4 *__restrict__ q,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Dynamic per-token activation quantization: one CTA per token row.
+//   pass 1: s[m] = max_k |x[m,k]| / QMAX (1 for an all-zero row)
+//   pass 2: codes Q(x / s[m]); OUT_BF16 writes INT8 codes as integer-valued BF16
+//           (the operand of the INT8 tensor-core path), else 1-byte codes.
+// The second pass re-reads the row (at most 38 KB) from L1/L2.
+// ---------------------------------------------------------------------------
+template <int QT, bool OUT_BF16>
+__global__ void __launch_bounds__(256) k_quantize_act_dyn(const uint16_t *__restrict__ x, float *__restrict__ s_out,
+                                                          void *__restrict__ q, int64_t K) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[8];
+  const int64_t m = blockIdx.x;
+  const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
+  const int64_t K8 = K / 8;
+  float amax = 0.0f;
+  for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      amax = fmaxf(amax, __uint_as_float((w[j] & 0x7FFFu) << 16));
+      amax = fmaxf(amax, __uint_as_float(w[j] & 0x7FFF0000u));
+    }
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+  const float sc = amax > 0.0f ? __fdiv_rn(amax, qmax_of(QT)) : 1.0f;
+  if (threadIdx.x == 0) s_out[m] = sc;
+  for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (OUT_BF16) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(w[j] & 0xFFFFu), sc);
+        const float hi = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(w[j] >> 16), sc);
+        o[j] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+      }
+      reinterpret_cast<uint4 *>((uint16_t *)q + m * K)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      uint32_t o[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t lo = w[2 * j], hi = w[2 * j + 1];
+        o[j] = (uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo & 0xFFFFu), sc) |
+               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo >> 16), sc) << 8) |
+               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi & 0xFFFFu), sc) << 16) |
+               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi >> 16), sc) << 24);
+      }
+      reinterpret_cast<uint2 *>((uint8_t *)q + m * K)[i] = make_uint2(o[0], o[1]);
+    }
+  }
+}
+
 // --------------------------------- launchers --------------------------------
 static int stream_grid(int64_t work, int per_cta, int sms) {
   int64_t g = (work + per_cta - 1) / per_cta;
@@ -218,5 +278,18 @@ cudaError_t launch_i8_to_bf16(int64_t M, int64_t K, const void *q, void *out, in
   if (n16 == 0) return cudaSuccess;
   return launch_kernel(k_i8_to_bf16, dim3(stream_grid(n16, 256, sms)), dim3(256), 0, st, 1, (const uint4 *)q,
                        (uint4 *)out, n16);
+}
+}  // namespace qlin
+
+namespace qlin {
+cudaError_t launch_quantize_act_dyn(int qtype, bool out_bf16, int64_t M, int64_t K, const void *x, float *s, void *q,
+                                    cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const dim3 grid((unsigned)M), block(256);
+  if (out_bf16)
+    return launch_kernel(k_quantize_act_dyn<QLIN_INT8, true>, grid, block, 0, st, 1, (const uint16_t *)x, s, q, K);
+  return qtype == QLIN_INT8
+             ? launch_kernel(k_quantize_act_dyn<QLIN_INT8, false>, grid, block, 0, st, 1, (const uint16_t *)x, s, q, K)
+             : launch_kernel(k_quantize_act_dyn<QLIN_E4M3, false>, grid, block, 0, st, 1, (const uint16_t *)x, s, q, K);
 }
 }  // namespace qlin

@@ -104,6 +104,7 @@ SMALL = "int8-w8a16-1k"            # INT8 W8A16, K=N=1024, M in {1,16}
 DECODE7B = "e4m3-w8a16-decode-7b"  # FP8-E4M3 W8A16 decode sweep, 7B-class shapes
 W8A8_3B = "int8-w8a8-static-3b"    # INT8 W8A8 static, 3B-class shapes, bias
 PREFILL = "e4m3-w8a8-static-prefill"  # FP8-E4M3 W8A8 static prefill
+W8A8_DYN_3B = "int8-w8a8-dynamic-3b"  # INT8 W8A8 with dynamic per-token scales, 3B-class shapes, bias
 STACK = "stack-36L-3b"             # 36-layer 3B linear stack, decode + prefill
 
 
@@ -122,6 +123,12 @@ def workload(name: str) -> Workload:
                   ("down_proj", 256, 11008, 2048), ("up_proj", 1024, 2048, 11008)]
         return Workload(name, "INT8 W8A8 static, 3B-class microbench shapes, bias",
                         [Linear(s, K, N, M, "int8", "w8a8", bias=True, workload=name)
+                         for (s, M, K, N) in shapes])
+    if name == W8A8_DYN_3B:
+        shapes = [("q_proj", 1, 2048, 2048), ("up_proj", 16, 2048, 11008),
+                  ("down_proj", 256, 11008, 2048), ("up_proj", 1024, 2048, 11008)]
+        return Workload(name, "INT8 W8A8 dynamic per-token, 3B-class microbench shapes, bias",
+                        [Linear(s, K, N, M, "int8", "w8a8dyn", bias=True, workload=name)
                          for (s, M, K, N) in shapes])
     if name == PREFILL:
         kn = [(2048, 11008), (11008, 2048), (2048, 2048)]
@@ -162,7 +169,7 @@ def make_inputs(lin: Linear, want=("w", "x", "cal", "bias"), x_rows: int | None 
     if "x" in want:
         M = lin.M if x_rows is None else x_rows
         out["x"] = activations(M, lin.K, rng_for(wl, L, f"{lin.name}.K{lin.K}.M{lin.M}", "act"), outl)
-    if "cal" in want and lin.form == "w8a8":
+    if "cal" in want and lin.form == "w8a8":  # static W8A8 only; the dynamic form needs no calibration
         out["cal"] = activations(CALIB_ROWS, lin.K, rng_for(wl, L, f"{lin.name}.K{lin.K}", "calib"), outl)
     if "bias" in want and lin.bias:
         out["bias"] = bias(lin.N, rng_for(wl, L, f"{lin.name}.N{lin.N}", "bias"))

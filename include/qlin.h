@@ -71,7 +71,8 @@ typedef enum {
   QLIN_OP_QUANTIZE_ACT = 2,
   QLIN_OP_W8A16_LINEAR = 3,
   QLIN_OP_W8A8_LINEAR = 4,
-  QLIN_OP_I8_GEMM_S32 = 5
+  QLIN_OP_I8_GEMM_S32 = 5,
+  QLIN_OP_W8A8_DYNAMIC_LINEAR = 6
 } qlin_op;
 
 /*
@@ -157,6 +158,31 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
                              const float *input_scale, const void *qw, const float *w_scale,
                              const void *bias, void *y, void *ws, size_t ws_bytes,
                              qlin_stream_t stream);
+
+/*
+ * Dynamic per-token activation quantization: the per-token abs-max scheme that
+ * "Nano-vLLM-MOE" README ("INT8 量化支持", 关键设计, W8A8 static item) contrasts
+ * with the static scalar (it costs one more reduction per token).  Per row m:
+ *   x_scale[m] = max_k |x[m,k]| / QMAX  (IEEE binary32 division; 1 for a zero row)
+ *   qx[m,k]    = INT8: clamp(round_half_even(x[m,k] / x_scale[m]), -127, 127)
+ *                E4M3: saturating round-half-even E4M3 cast of x[m,k] / x_scale[m]
+ *   x [M,K] BF16, qx [M,K] 1-byte codes, x_scale [M] fp32 (all device).
+ * Requirements: M >= 0, K >= 16, K % 16 == 0, pointers 16-byte aligned.
+ */
+qlin_status qlin_quantize_act_dynamic(qlin_qtype qtype, int64_t M, int64_t K, const void *x, void *qx,
+                                      float *x_scale, qlin_stream_t stream);
+
+/*
+ * W8A8 linear with dynamic per-token activation scales (same reading as above):
+ *   qx, s_x = quantize_act_dynamic(x)                    (into the workspace)
+ *   y[m,n]  = bf16( acc[m,n] * (s_x[m] * w_scale[n]) + bias[n] )
+ * with acc as in qlin_w8a8_linear (exact int32 for INT8, fp32 for E4M3).
+ *   ws: qlin_workspace_bytes(QLIN_OP_W8A8_DYNAMIC_LINEAR, qtype, M, K, N) bytes.
+ * Requirements as for qlin_w8a16_linear.
+ */
+qlin_status qlin_w8a8_dynamic_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
+                                     const void *qw, const float *w_scale, const void *bias, void *y, void *ws,
+                                     size_t ws_bytes, qlin_stream_t stream);
 
 /*
  * Raw INT8 GEMM accumulator, the integer core of the INT8 W8A8 linear, exposed
