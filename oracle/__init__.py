@@ -3,7 +3,9 @@
 A plain CPU restatement (C, fp64 / exact integer arithmetic) of the 8-bit
 quantized linear layer: per-output-channel weight quantizers (INT8 and OCP
 E4M3), the static activation scale from a calibration batch, static activation
-quantization, the exact INT8 accumulator and the fp64 W8A8 / W8A16 references.
+quantization, the exact INT8 accumulator, the fp64 W8A8 / W8A16 references and
+the mixed KV-cache quantizers (INT8 keys with float16 group scales, E4M3 values
+with float16 per-token scales).
 The C source ``qlin_oracle.c`` cites the passages it follows.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
@@ -67,6 +69,16 @@ def lib() -> ctypes.CDLL:
             L.orc_quantize_act_per_token.restype = None
             L.orc_w8a8_per_token.argtypes = [I, I64, I64, I64, P, P, P, P, P, P, I64, P]
             L.orc_w8a8_per_token.restype = None
+            L.orc_fp16_decode.argtypes = [ctypes.c_uint16]
+            L.orc_fp16_decode.restype = ctypes.c_double
+            L.orc_fp16_encode.argtypes = [ctypes.c_double]
+            L.orc_fp16_encode.restype = ctypes.c_uint16
+            L.orc_bf16_encode.argtypes = [ctypes.c_double]
+            L.orc_bf16_encode.restype = ctypes.c_uint16
+            L.orc_kv_store.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64, P, P, P, P]
+            L.orc_kv_store.restype = I64
+            L.orc_kv_load.argtypes = [I64, I64, I64, P, I64, P, P, P, P, P, P]
+            L.orc_kv_load.restype = I64
             L.orc_num_threads.argtypes = []
             L.orc_num_threads.restype = I
             _lib = L
@@ -191,6 +203,62 @@ def w8a8_per_token(qtype: int, qx, s_x, qw, s_w, bias=None, rows=None) -> np.nda
     lib().orc_w8a8_per_token(qtype, M, K, N, _ptr(qx), _ptr(s_x), _ptr(qw), _ptr(s_w), _ptr(b), _ptr(r), R,
                              _ptr(y))
     return y
+
+
+def fp16_decode(code: int) -> float:
+    return lib().orc_fp16_decode(int(code) & 0xFFFF)
+
+
+def fp16_encode(v: float) -> int:
+    return int(lib().orc_fp16_encode(float(v)))
+
+
+def bf16_encode(v: float) -> int:
+    return int(lib().orc_bf16_encode(float(v)))
+
+
+class KVCache:
+    """Host copy of a mixed KV cache with num_slots slots, H kv heads and head
+    size D: k_cache int8 bits [S,H,D], k_scale float16 bits [S,H,D/32], v_cache
+    E4M3 codes [S,H,D], v_scale float16 bits [S,H].  Every byte starts as `fill`."""
+
+    def __init__(self, num_slots: int, H: int, D: int, fill: int = 0):
+        assert D % 32 == 0
+        self.num_slots, self.H, self.D = num_slots, H, D
+        self.k_cache = np.full((num_slots, H, D), fill & 0xFF, np.uint8)
+        self.k_scale = np.full((num_slots, H, D // 32), (fill & 0xFF) * 0x0101, np.uint16)
+        self.v_cache = np.full((num_slots, H, D), fill & 0xFF, np.uint8)
+        self.v_scale = np.full((num_slots, H), (fill & 0xFF) * 0x0101, np.uint16)
+
+    def nbytes(self) -> int:
+        return sum(a.nbytes for a in (self.k_cache, self.k_scale, self.v_cache, self.v_scale))
+
+
+def kv_store(cache: KVCache, k_bf16, v_bf16, slots) -> int:
+    """Quantizes token rows k, v (uint16 BF16 bits [T, ld >= H*D]) into cache
+    slots; negative slots are skipped.  Returns the count of slots >= num_slots."""
+    k = _c(k_bf16, np.uint16)
+    v = _c(v_bf16, np.uint16)
+    sl = _c(np.asarray(slots, np.int64), np.int64)
+    T = sl.shape[0]
+    H, D = cache.H, cache.D
+    assert k.shape[0] == T and v.shape[0] == T and k.shape[1] >= H * D and v.shape[1] >= H * D
+    return int(lib().orc_kv_store(T, H, D, _ptr(k), k.shape[1], _ptr(v), v.shape[1], _ptr(sl), cache.num_slots,
+                                  _ptr(cache.k_cache), _ptr(cache.k_scale), _ptr(cache.v_cache),
+                                  _ptr(cache.v_scale)))
+
+
+def kv_load(cache: KVCache, slots):
+    """Dequantizes cache slots to BF16 bits (k_out, v_out) [T,H,D] and the count
+    of slots >= num_slots; negative or out-of-range slots give rows of +0."""
+    sl = _c(np.asarray(slots, np.int64), np.int64)
+    T = sl.shape[0]
+    H, D = cache.H, cache.D
+    ko = np.empty((T, H, D), np.uint16)
+    vo = np.empty((T, H, D), np.uint16)
+    bad = lib().orc_kv_load(T, H, D, _ptr(sl), cache.num_slots, _ptr(cache.k_cache), _ptr(cache.k_scale),
+                            _ptr(cache.v_cache), _ptr(cache.v_scale), _ptr(ko), _ptr(vo))
+    return ko, vo, int(bad)
 
 
 def num_threads() -> int:

@@ -275,3 +275,147 @@ int orc_num_threads(void) {
   return 1;
 #endif
 }
+
+/* ---- mixed KV-cache quantization -----------------------------------------
+ * "Nano-vLLM-MoE" README (English), section "KV cache compression" (Setup and
+ * the memory table) and the Highlights list: keys are stored as INT8 with one
+ * float16 scale per group of 32 consecutive head_dim elements, values as FP8
+ * (E4M3) with one dynamic float16 scale per token and kv head.  This layout is
+ * the one whose size matches the printed 0.5195x BF16 bytes per block and the
+ * 7.00 -> 3.64 GiB arena of a 7B model (4 kv heads, head_dim 128).
+ * Readings where the page is silent:
+ *   - scale = RN_fp16(fl32(amax / QMAX)): an fp32 division, then the float16
+ *     cast of that quotient; magnitudes beyond 65504 saturate to 65504;
+ *   - a scale that is zero after the cast (all-zero group, or amax so small
+ *     that amax/QMAX underflows float16) is replaced by 1.0, so the codes are 0;
+ *   - codes quantize with the stored float16 scale: q = Q(fl32(x / s16));
+ *   - dequantized values are the exact product q * s16 rounded once to BF16. */
+
+/* Nearest value to a >= 0 on a binary grid with P significant bits whose
+ * smallest normal exponent is EMIN (subnormals below it), ties to the even
+ * last bit.  The grid spacing in the binade [2^E, 2^(E+1)) is 2^(E-P+1). */
+static double round_to_grid(double a, int P, int EMIN) {
+  if (a == 0.0) return 0.0;
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;
+  if (E < EMIN) E = EMIN;
+  double quantum = ldexp(1.0, E - P + 1);
+  return nearbyint(a / quantum) * quantum; /* a/quantum is exact (power of two) */
+}
+
+/* IEEE binary16: bias 15, 10 stored mantissa bits, subnormal step 2^-24,
+ * largest finite 65504.  Exact value of a finite code (NaN/Inf map to NaN/Inf). */
+double orc_fp16_decode(uint16_t h) {
+  int s = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+  double v;
+  if (e == 31) v = m ? NAN : INFINITY;
+  else v = (e == 0) ? ldexp((double)m, -24) : ldexp((double)(1024 + m), e - 25);
+  return s ? -v : v;
+}
+
+/* Nearest binary16 code to a finite v, ties to even, saturating at +-65504,
+ * sign of zero kept. */
+uint16_t orc_fp16_encode(double v) {
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = round_to_grid(fabs(v), 11, -14);
+  if (a >= 65504.0) return sign | 0x7BFF;
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;
+  if (E < -14) return sign | (uint16_t)(a / ldexp(1.0, -24)); /* subnormal */
+  int mfield = (int)(a / ldexp(1.0, E - 10)) - 1024;
+  return sign | (uint16_t)(((E + 15) << 10) | mfield);
+}
+
+/* BF16 (the upper half of binary32: 8 significant bits, exponent range of
+ * fp32) nearest to a finite v inside the binary32 range, ties to even. */
+uint16_t orc_bf16_encode(double v) {
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = round_to_grid(fabs(v), 8, -126);
+  float f = (float)a; /* exact: a lies on the BF16 grid */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return sign | (uint16_t)(u >> 16);
+}
+
+static uint16_t kv_scale16(float amax, float qmax) {
+  float s32 = amax / qmax; /* IEEE binary32 division */
+  uint16_t h = orc_fp16_encode((double)s32);
+  if ((h & 0x7FFF) == 0) h = 0x3C00; /* 1.0 */
+  return h;
+}
+
+/* Quantizes the T token rows of k and v (BF16, row t at k + t*ldk, holding H
+ * heads of D elements each; D a multiple of 32) into the slots slots[t] of a
+ * cache with num_slots slots:
+ *   k_cache[slot][h][d] int8, k_scale[slot][h][d/32] float16 bits,
+ *   v_cache[slot][h][d] E4M3, v_scale[slot][h] float16 bits.
+ * A negative slot skips the token.  Returns the number of tokens whose slot is
+ * >= num_slots (those are skipped too). */
+int64_t orc_kv_store(int64_t T, int64_t H, int64_t D, const uint16_t *k, int64_t ldk,
+                     const uint16_t *v, int64_t ldv, const int64_t *slots, int64_t num_slots,
+                     uint8_t *k_cache, uint16_t *k_scale, uint8_t *v_cache, uint16_t *v_scale) {
+  const int64_t G = D / 32;
+  int64_t bad = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t slot = slots[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) { ++bad; continue; }
+    for (int64_t h = 0; h < H; ++h) {
+      const uint16_t *kr = k + t * ldk + h * D;
+      const uint16_t *vr = v + t * ldv + h * D;
+      uint8_t *kq = k_cache + (slot * H + h) * D;
+      uint8_t *vq = v_cache + (slot * H + h) * D;
+      for (int64_t g = 0; g < G; ++g) {
+        float amax = 0.0f;
+        for (int64_t d = 32 * g; d < 32 * g + 32; ++d) {
+          float a = fabsf(bf16_to_f32(kr[d]));
+          if (a > amax) amax = a;
+        }
+        uint16_t s16 = kv_scale16(amax, 127.0f);
+        k_scale[(slot * H + h) * G + g] = s16;
+        float s = (float)orc_fp16_decode(s16);
+        for (int64_t d = 32 * g; d < 32 * g + 32; ++d) kq[d] = quantize_value(ORC_INT8, bf16_to_f32(kr[d]), s);
+      }
+      float amax = 0.0f;
+      for (int64_t d = 0; d < D; ++d) {
+        float a = fabsf(bf16_to_f32(vr[d]));
+        if (a > amax) amax = a;
+      }
+      uint16_t s16 = kv_scale16(amax, 448.0f);
+      v_scale[slot * H + h] = s16;
+      float s = (float)orc_fp16_decode(s16);
+      for (int64_t d = 0; d < D; ++d) vq[d] = quantize_value(ORC_E4M3, bf16_to_f32(vr[d]), s);
+    }
+  }
+  return bad;
+}
+
+/* Reads slots[t] of the cache back as BF16 rows k_out[t][h][d], v_out[t][h][d]
+ * (row stride H*D): value = RN_bf16(code * scale), exact product.  A negative
+ * slot yields a row of +0.  Returns the number of slots >= num_slots (their
+ * rows are left as +0 too). */
+int64_t orc_kv_load(int64_t T, int64_t H, int64_t D, const int64_t *slots, int64_t num_slots,
+                    const uint8_t *k_cache, const uint16_t *k_scale, const uint8_t *v_cache,
+                    const uint16_t *v_scale, uint16_t *k_out, uint16_t *v_out) {
+  const int64_t G = D / 32;
+  int64_t bad = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t slot = slots[t];
+    int ok = slot >= 0 && slot < num_slots;
+    if (slot >= num_slots) ++bad;
+    for (int64_t h = 0; h < H; ++h)
+      for (int64_t d = 0; d < D; ++d) {
+        int64_t o = (t * H + h) * D + d;
+        if (!ok) { k_out[o] = 0; v_out[o] = 0; continue; }
+        int64_t c = (slot * H + h) * D + d;
+        double ks = orc_fp16_decode(k_scale[(slot * H + h) * G + d / 32]);
+        double vs = orc_fp16_decode(v_scale[slot * H + h]);
+        k_out[o] = orc_bf16_encode((double)(int8_t)k_cache[c] * ks);
+        v_out[o] = orc_bf16_encode(orc_e4m3_decode(v_cache[c]) * vs);
+      }
+  }
+  return bad;
+}
