@@ -30,11 +30,45 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// One quantization step q = Q(x / s): IEEE binary32 division, then
-// INT8: round half to even + clamp to [-127,127];  E4M3: saturating RNE cast.
-template <int QT>
-__device__ __forceinline__ uint8_t quantize_one(float x, float s) {
-  float v = __fdiv_rn(x, s);
+// A quantization scale s > 0 with its correctly rounded reciprocal r = RN(1/s).
+// `fast` holds when s lies in [2^-96, 2^96]: then 1/s and every intermediate of
+// quotient() below stay in the normal range.
+struct Scale {
+  float s, r;
+  bool fast;
+};
+__device__ __forceinline__ Scale make_scale(float s) {
+  return Scale{s, __frcp_rn(s), s >= 0x1p-96f && s <= 0x1p96f};
+}
+
+// x / s correctly rounded to binary32, computed from r instead of a division
+// per element, by Markstein's theorem (P. W. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): if r is within half an ulp of 1/s and q within one ulp
+// of x/s, the residual x - q*s is exact in one FMA and RN(q + residual * r)
+// is RN(x/s), barring overflow and underflow.  q = RN(x*r) is within one ulp.
+//   - BOUNDED callers derive s from the abs-max of the very values they divide,
+//     so |x/s| is about QMAX and nothing overflows.  Otherwise (a static scale
+//     at run time) q is first clamped to +-2^32: every code beyond that clamps
+//     or saturates anyway, and the clamp keeps the residual finite.
+//   - A quotient in the subnormal range gives code 0 whatever its last bits;
+//     its sign (that of x, s > 0) is restored by copysign, which also keeps
+//     the sign of a zero x that the correction step would lose.
+//   - Scales outside [2^-96, 2^96] take the IEEE division.
+template <bool BOUNDED>
+__device__ __forceinline__ float quotient(float x, const Scale &c) {
+  if (!c.fast) return __fdiv_rn(x, c.s);
+  float q = __fmul_rn(x, c.r);
+  if constexpr (!BOUNDED) q = fminf(fmaxf(q, -0x1p32f), 0x1p32f);
+  const float rem = __fmaf_rn(-q, c.s, x);
+  return copysignf(__fmaf_rn(rem, c.r, q), x);
+}
+
+// One quantization step q = Q(x / s): the correctly rounded binary32 quotient,
+// then INT8: round half to even + clamp to [-127,127];  E4M3: saturating RNE cast.
+template <int QT, bool BOUNDED>
+__device__ __forceinline__ uint8_t quantize_one(float x, const Scale &c) {
+  const float v = quotient<BOUNDED>(x, c);
   if constexpr (QT == QLIN_INT8) {
     float r = fminf(fmaxf(rintf(v), -127.0f), 127.0f);
     return (uint8_t)(int8_t)__float2int_rn(r);

@@ -1,6 +1,7 @@
 // Quantizers: per-output-channel weight quantization, calibration abs-max and
 // static per-tensor activation quantization.  All HBM-streaming kernels with
-// 16-byte vector accesses; the arithmetic of one element is qlin::quantize_one.
+// 16-byte vector accesses; the arithmetic of one element is qlin::quantize_one
+// (the quotient by the scale correctly rounded, then the code).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -34,15 +35,16 @@ __global__ void __launch_bounds__(256) k_quantize_weight(const float *__restrict
   for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
   const float sc = amax > 0.0f ? __fdiv_rn(amax, qmax_of(QT)) : 1.0f;
   if (threadIdx.x == 0) s[n] = sc;
+  const Scale scl = make_scale(sc);
   uint4 *qrow = reinterpret_cast<uint4 *>(q + n * K);
   for (int64_t i = threadIdx.x; i < K16; i += blockDim.x) {
     uint32_t out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float4 v = __ldg(row + 4 * i + j);
-      out[j] = (uint32_t)quantize_one<QT>(v.x, sc) | ((uint32_t)quantize_one<QT>(v.y, sc) << 8) |
-               ((uint32_t)quantize_one<QT>(v.z, sc) << 16) |
-               ((uint32_t)quantize_one<QT>(v.w, sc) << 24);
+      out[j] = (uint32_t)quantize_one<QT, true>(v.x, scl) | ((uint32_t)quantize_one<QT, true>(v.y, scl) << 8) |
+               ((uint32_t)quantize_one<QT, true>(v.z, scl) << 16) |
+               ((uint32_t)quantize_one<QT, true>(v.w, scl) << 24);
     }
     qrow[i] = make_uint4(out[0], out[1], out[2], out[3]);
   }
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ 
                                                       uint4 *__restrict__ q, int64_t n16) {
   pdl_wait();
   pdl_trigger();
-  const float s = __ldg(s_ptr);
+  const Scale s = make_scale(__ldg(s_ptr));
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
        i += (int64_t)gridDim.x * blockDim.x) {
     uint4 a = __ldg(x + 2 * i), b = __ldg(x + 2 * i + 1);
@@ -107,10 +109,10 @@ __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t lo = in[2 * j], hi = in[2 * j + 1];
-      out[j] = (uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo & 0xFFFFu), s) |
-               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo >> 16), s) << 8) |
-               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi & 0xFFFFu), s) << 16) |
-               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi >> 16), s) << 24);
+      out[j] = (uint32_t)quantize_one<QT, false>(bf16_bits_to_f32(lo & 0xFFFFu), s) |
+               ((uint32_t)quantize_one<QT, false>(bf16_bits_to_f32(lo >> 16), s) << 8) |
+               ((uint32_t)quantize_one<QT, false>(bf16_bits_to_f32(hi & 0xFFFFu), s) << 16) |
+               ((uint32_t)quantize_one<QT, false>(bf16_bits_to_f32(hi >> 16), s) << 24);
     }
     q[i] = make_uint4(out[0], out[1], out[2], out[3]);
   }
@@ -125,14 +127,14 @@ __global__ void __launch_bounds__(256) k_quantize_act_i8bf16(const uint4 *__rest
                                                             uint4 *__restrict__ q, int64_t n8) {
   pdl_wait();
   pdl_trigger();
-  const float s = __ldg(s_ptr);
+  const Scale s = make_scale(__ldg(s_ptr));
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
     const uint4 a = __ldg(x + i);
     uint32_t in[4] = {a.x, a.y, a.z, a.w}, out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float lo = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(in[j] & 0xFFFFu), s);
-      const float hi = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(in[j] >> 16), s);
+      const float lo = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(in[j] & 0xFFFFu), s);
+      const float hi = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(in[j] >> 16), s);
       out[j] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
     }
     q[i] = make_uint4(out[0], out[1], out[2], out[3]);
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(256) k_quantize_act_dyn(const uint16_t *__rest
   for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
   const float sc = amax > 0.0f ? __fdiv_rn(amax, qmax_of(QT)) : 1.0f;
   if (threadIdx.x == 0) s_out[m] = sc;
+  const Scale scl = make_scale(sc);
   for (int64_t i = threadIdx.x; i < K8; i += blockDim.x) {
     const uint4 v = __ldg(row + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -202,8 +205,8 @@ __global__ void __launch_bounds__(256) k_quantize_act_dyn(const uint16_t *__rest
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float lo = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(w[j] & 0xFFFFu), sc);
-        const float hi = (float)(int8_t)quantize_one<QLIN_INT8>(bf16_bits_to_f32(w[j] >> 16), sc);
+        const float lo = (float)(int8_t)quantize_one<QLIN_INT8, true>(bf16_bits_to_f32(w[j] & 0xFFFFu), scl);
+        const float hi = (float)(int8_t)quantize_one<QLIN_INT8, true>(bf16_bits_to_f32(w[j] >> 16), scl);
         o[j] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
       }
       reinterpret_cast<uint4 *>((uint16_t *)q + m * K)[i] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -212,10 +215,10 @@ __global__ void __launch_bounds__(256) k_quantize_act_dyn(const uint16_t *__rest
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const uint32_t lo = w[2 * j], hi = w[2 * j + 1];
-        o[j] = (uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo & 0xFFFFu), sc) |
-               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(lo >> 16), sc) << 8) |
-               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi & 0xFFFFu), sc) << 16) |
-               ((uint32_t)quantize_one<QT>(bf16_bits_to_f32(hi >> 16), sc) << 24);
+        o[j] = (uint32_t)quantize_one<QT, true>(bf16_bits_to_f32(lo & 0xFFFFu), scl) |
+               ((uint32_t)quantize_one<QT, true>(bf16_bits_to_f32(lo >> 16), scl) << 8) |
+               ((uint32_t)quantize_one<QT, true>(bf16_bits_to_f32(hi & 0xFFFFu), scl) << 16) |
+               ((uint32_t)quantize_one<QT, true>(bf16_bits_to_f32(hi >> 16), scl) << 24);
       }
       reinterpret_cast<uint2 *>((uint8_t *)q + m * K)[i] = make_uint2(o[0], o[1]);
     }
