@@ -60,6 +60,8 @@ def workload_calls(name: str):
         return synth.stack_linears("decode"), synth.STACK + "-decode"
     if name == "stack-prefill":
         return synth.stack_linears("prefill"), synth.STACK + "-prefill"
+    if name == "kv7b":
+        return [], synth.KV7B
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -269,20 +271,41 @@ class GpuWorkload:
         op = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR,
               "w8a8dyn": capi.QLIN_OP_W8A8_DYNAMIC_LINEAR}
         self.kernel = [capi.qlin_kernel_name(op[l.form], l.qtype, l.M, l.K, l.N) for l in self.lins]
+        self.set_accounting()
 
-    def _capture(self, copy, events=None, e2e=False):
+    def set_accounting(self):
+        """Per-call algorithmic bytes / flops, the tensor peak each call is bound by,
+        a description of each call, and the host<->device copies of the e2e step."""
+        self.call_bytes = [alg_bytes(l) for l in self.lins]
+        self.call_flops = [alg_flops(l) for l in self.lins]
+        self.call_fp8 = [l.form == "w8a8" and l.qtype == "e4m3" for l in self.lins]
+        self.call_info = [{"name": l.name, "M": l.M, "K": l.K, "N": l.N} for l in self.lins]
+        self.h2d = [(self.x[i], self.x_host[i]) for i in range(len(self.lins))]
+        self.d2h = [(self.y_host[i], self.y[i]) for i in range(len(self.lins))]
+        l0 = self.lins[0]
+        self.dtype = (("e4m3" if l0.qtype == "e4m3" else "int8") + ("xbf16" if l0.form == "w8a16" else "")
+                      + "->f32acc->bf16")
+        self.extra_config = {"linears": len(self.lins), "weight_bytes": self.weight_bytes,
+                             "weight_copies": self.copies,
+                             "l2": (f"{self.copies} alternating weight copies of {self.weight_bytes / 1e6:.0f} MB "
+                                    f"each (L2 is {L2_BYTES / 2**20:.0f} MiB)")}
+
+    def _capture(self, copy, events=None, e2e=False, only=None):
         """CUDA graph of one step on weight copy `copy` (PDL edges between the
         kernels); with `events`, each call is bracketed by external event nodes;
         with `e2e`, host->device copies of the activations and device->host
-        copies of the outputs are part of the graph."""
+        copies of the outputs are part of the graph; with `only` (a kernel
+        name), just the calls that launch that kernel, in step order."""
         torch = self.torch
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.stream):
             if e2e:
-                for i in range(len(self.lins)):
-                    self.x[i].copy_(self.x_host[i], non_blocking=True)
+                for dst, src in self.h2d:
+                    dst.copy_(src, non_blocking=True)
             args = self.args[copy]
             for i, fn in enumerate(self.fns):
+                if only is not None and self.kernel[i] != only:
+                    continue
                 if events is not None:
                     events[i][0].record(self.stream)
                 st = fn(*args[i])
@@ -291,8 +314,8 @@ class GpuWorkload:
                 if st != 0:
                     raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
             if e2e:
-                for i in range(len(self.lins)):
-                    self.y_host[i].copy_(self.y[i], non_blocking=True)
+                for dst, src in self.d2h:
+                    dst.copy_(src, non_blocking=True)
         return g
 
     def build_graphs(self, with_events):
@@ -307,8 +330,9 @@ class GpuWorkload:
         self.events = None
         if with_events:
             self.events = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                            for _ in self.lins] for _ in range(self.copies)]
+                            for _ in self.fns] for _ in range(self.copies)]
             self.graphs_ev = [self._capture(c, events=self.events[c]) for c in range(self.copies)]
+        self.graphs_kernel = {k: [self._capture(c, only=k) for c in range(self.copies)] for k in set(self.kernel)}
         torch.cuda.synchronize()
 
     def run_step(self, step, ev=None):
@@ -323,11 +347,101 @@ class GpuWorkload:
                 raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
 
     def run_step_e2e(self, step):
-        for i in range(len(self.lins)):
-            self.x[i].copy_(self.x_host[i], non_blocking=True)
+        for dst, src in self.h2d:
+            dst.copy_(src, non_blocking=True)
         self.run_step(step)
-        for i in range(len(self.lins)):
-            self.y_host[i].copy_(self.y[i], non_blocking=True)
+        for dst, src in self.d2h:
+            dst.copy_(src, non_blocking=True)
+
+
+def kv_bytes(T, H, D, store):
+    """Algorithmic bytes of one KV-cache call over T tokens: BF16 rows (2 B/element,
+    keys and values), codes (1 B/element), float16 scales (D/32 + 1 per token-head)
+    and the int64 slot of each token."""
+    bf16 = 2 * T * H * D * 2
+    quant = 2 * T * H * D + 2 * T * H * (D // 32 + 1)
+    return bf16 + quant + 8 * T
+
+
+class KvWorkload(GpuWorkload):
+    """Mixed KV-cache step of a 7B model: per layer, quantize an 8192-token prefill
+    chunk into its cache blocks (qlin_kv_store_mixed) and read the layer's whole
+    32768-token context back as BF16 (qlin_kv_load_mixed)."""
+
+    def __init__(self, name, dev):
+        import torch
+        from bit_quantized_linear_gb300 import capi
+        self.torch, self.capi = torch, capi
+        self.name, self.dev, self.copies = name, dev, 1
+        self.lins, self.wl = [], synth.KV7B
+        L = capi.lib()
+        H, D, S, T = synth.KV_HEADS, synth.KV_HEAD_DIM, synth.KV_CONTEXT, synth.KV_CHUNK
+        self.stream = torch.cuda.current_stream()
+        sp = ctypes.c_void_p(self.stream.cuda_stream)
+        P = ctypes.c_void_p
+
+        def dev_normal(shape, layer, role):
+            g = torch.Generator(device=dev)
+            g.manual_seed(synth.sub_seed(synth.KV7B, layer, role, "act") % (2 ** 63))
+            return torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+        self.caches, self.k_new, self.v_new, self.chunk_slots, self.ctx_slots = [], [], [], [], []
+        for layer in range(synth.KV_LAYERS):
+            cache = capi.kv_cache_alloc(S, H, D, device=dev)
+            ctx = torch.from_numpy(synth.kv_context_slots(layer)).to(dev)
+            # the context already in the cache before the step
+            kf, vf = dev_normal((S, H * D), layer, "k.ctx"), dev_normal((S, H * D), layer, "v.ctx")
+            capi.qlin_kv_store_mixed(kf, vf, ctx, *cache)
+            del kf, vf
+            self.caches.append(cache)
+            self.ctx_slots.append(ctx)
+            self.chunk_slots.append(torch.from_numpy(synth.kv_chunk_slots(layer)).to(dev))
+            self.k_new.append(dev_normal((T, H * D), layer, "k.chunk"))
+            self.v_new.append(dev_normal((T, H * D), layer, "v.chunk"))
+        self.k_out = torch.empty((S, H, D), dtype=torch.bfloat16, device=dev)
+        self.v_out = torch.empty((S, H, D), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        if capi.qlin_get_device_status() != capi.QLIN_OK:
+            raise RuntimeError("KV cache fill reported an error")
+        self.k_new_host = [t.cpu().pin_memory() for t in self.k_new]
+        self.v_new_host = [t.cpu().pin_memory() for t in self.v_new]
+        self.k_out_host = torch.empty((S, H, D), dtype=torch.bfloat16).pin_memory()
+        self.v_out_host = torch.empty((S, H, D), dtype=torch.bfloat16).pin_memory()
+
+        def ptr(t):
+            return P(t.data_ptr())
+
+        self.fns, self.args, self.kernel = [], [[]], []
+        self.call_bytes, self.call_flops, self.call_fp8, self.call_info = [], [], [], []
+        store_name = capi.qlin_kernel_name(capi.QLIN_OP_KV_STORE_MIXED, 0, T, D, H)
+        load_name = capi.qlin_kernel_name(capi.QLIN_OP_KV_LOAD_MIXED, 0, S, D, H)
+        for layer in range(synth.KV_LAYERS):
+            kc, ks, vc, vs = (ptr(a) for a in self.caches[layer])
+            self.fns.append(L.qlin_kv_store_mixed)
+            self.args[0].append((T, H, D, ptr(self.k_new[layer]), H * D, ptr(self.v_new[layer]), H * D,
+                                 ptr(self.chunk_slots[layer]), S, kc, ks, vc, vs, sp))
+            self.kernel.append(store_name)
+            self.call_bytes.append(kv_bytes(T, H, D, True))
+            self.call_info.append({"name": f"L{layer}.kv_store", "T": T, "H": H, "D": D})
+            self.fns.append(L.qlin_kv_load_mixed)
+            self.args[0].append((S, H, D, ptr(self.ctx_slots[layer]), S, kc, ks, vc, vs, ptr(self.k_out),
+                                 ptr(self.v_out), sp))
+            self.kernel.append(load_name)
+            self.call_bytes.append(kv_bytes(S, H, D, False))
+            self.call_info.append({"name": f"L{layer}.kv_load", "T": S, "H": H, "D": D})
+        self.call_flops = [0] * len(self.fns)
+        self.call_fp8 = [False] * len(self.fns)
+        # e2e: the new tokens come from the host; the last layer's dequantized context goes back
+        self.h2d = [(self.k_new[i], self.k_new_host[i]) for i in range(synth.KV_LAYERS)] + \
+                   [(self.v_new[i], self.v_new_host[i]) for i in range(synth.KV_LAYERS)]
+        self.d2h = [(self.k_out_host, self.k_out), (self.v_out_host, self.v_out)]
+        self.dtype = "bf16->int8|e4m3 codes+f16 scales->bf16"
+        cache_bytes = sum(a.numel() * a.element_size() for c in self.caches for a in c)
+        self.weight_bytes = cache_bytes
+        self.extra_config = {"layers": synth.KV_LAYERS, "kv_heads": H, "head_dim": D, "block_size": synth.KV_BLOCK,
+                             "chunk_tokens": T, "context_tokens": S, "cache_bytes": cache_bytes,
+                             "l2": f"{cache_bytes / 1e6:.0f} MB of KV cache per step (L2 is "
+                                   f"{L2_BYTES / 2**20:.0f} MiB)"}
 
 
 def kernel_digest() -> str:
@@ -354,10 +468,34 @@ def traffic_for(kernel: str, wl: str):
 
 
 # ---------------------------------------------------------------- CPU side
+def oracle_kv_sample():
+    """Bounded oracle sample of the KV step: layer 0's store of the first 2048
+    chunk tokens and load of the first 4096 context tokens."""
+    import oracle
+    H, D, S = synth.KV_HEADS, synth.KV_HEAD_DIM, synth.KV_CONTEXT
+    Ts, Tl = 2048, 4096
+    k = synth.kv_tokens(0, Ts, "k")
+    v = synth.kv_tokens(0, Ts, "v")
+    chunk = synth.kv_chunk_slots(0)[:Ts]
+    ctx = synth.kv_context_slots(0)[:Tl]
+    cache = oracle.KVCache(S, H, D)
+    oracle.kv_store(cache, synth.kv_tokens(0, Tl, "k.ctx"), synth.kv_tokens(0, Tl, "v.ctx"), ctx)
+
+    def run():
+        oracle.kv_store(cache, k, v, chunk)
+        oracle.kv_load(cache, ctx)
+
+    units = kv_bytes(Ts, H, D, True) + kv_bytes(Tl, H, D, False)
+    desc = f"layer 0: store of {Ts} chunk tokens + load of {Tl} context tokens (H={H}, D={D}), single thread"
+    return run, units, desc, 1
+
+
 def oracle_sample(name, rows_per_call=1):
     """Bounded oracle sample of one step: every linear of the workload, first
     `rows_per_call` output rows (the oracle still streams the whole weight)."""
     import oracle
+    if name == "kv7b":
+        return oracle_kv_sample()
     lins, wl = workload_calls(name)
     if name.startswith("stack"):
         lins = lins[:6]  # one layer of the stack
@@ -433,7 +571,7 @@ def main():
     ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     ap.add_argument("--workload", default="decode7b",
                     choices=["decode7b", "small", "w8a8-3b", "w8a8-dyn-3b", "prefill", "stack-decode",
-                             "stack-prefill"])
+                             "stack-prefill", "kv7b"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
@@ -447,6 +585,8 @@ def main():
     metric_unit = "TFLOP/s" if prefill else "GB/s"
     metric = ("quantized-linear TOPS (prefill), % of roofline" if prefill
               else "quantized-linear GB/s (decode M<=256), % of roofline")
+    if a.workload == "kv7b":
+        metric = "mixed KV-cache quantize+dequantize GB/s, % of roofline"
     lins, wl = workload_calls(a.workload)
     unit_scale = 1e12 if prefill else 1e9
 
@@ -480,11 +620,11 @@ def main():
     dev = torch.device("cuda", local)
     from bit_quantized_linear_gb300 import capi
 
-    W = GpuWorkload(a.workload, dev)
-    n = len(W.lins)
-    units_step = sum(alg_flops(l) if prefill else alg_bytes(l) for l in W.lins)
-    bytes_step = sum(alg_bytes(l) for l in W.lins)
-    flops_step = sum(alg_flops(l) for l in W.lins)
+    W = KvWorkload(a.workload, dev) if a.workload == "kv7b" else GpuWorkload(a.workload, dev)
+    n = len(W.fns)
+    units_step = sum(W.call_flops) if prefill else sum(W.call_bytes)
+    bytes_step = sum(W.call_bytes)
+    flops_step = sum(W.call_flops)
 
     def barrier():
         if world > 1:
@@ -544,14 +684,33 @@ def main():
         timing = "stream events around each launch"
     mean_call = dur.mean(axis=0)
     per_kernel = {}
-    for i, l in enumerate(W.lins):
+    for i in range(n):
         k = W.kernel[i]
         d = per_kernel.setdefault(k, {"time": 0.0, "bytes": 0, "flops": 0, "calls": 0})
         d["time"] += mean_call[i]
-        d["bytes"] += alg_bytes(l)
-        d["flops"] += alg_flops(l)
+        d["bytes"] += W.call_bytes[i]
+        d["flops"] += W.call_flops[i]
         d["calls"] += 1
     dom = max(per_kernel, key=lambda k: per_kernel[k]["time"])
+    # ---- timed region 3: each kernel alone, its calls back to back in one graph ----
+    # (no event nodes between launches, so consecutive launches overlap prologue and
+    # tail through programmatic dependent launch as they do inside a step)
+    reps = max(3, min(a.steps, 200))
+    for k, gl in W.graphs_kernel.items():
+        for r in range(a.warmup):
+            gl[r % W.copies].replay()
+        torch.cuda.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(W.stream)
+        for r in range(reps):
+            gl[r % W.copies].replay()
+        k1.record(W.stream)
+        torch.cuda.synchronize()
+        per_kernel[k]["graph_time"] = k0.elapsed_time(k1) / 1e3 / reps  # seconds per pass over its calls
+        # bytes the alternating passes stream; below ~1.5x L2 a pass can be served from L2
+        per_kernel[k]["graph_trusted"] = per_kernel[k]["bytes"] * W.copies > 1.5 * L2_BYTES
+    for k, v in per_kernel.items():
+        v["launch_time"] = v["graph_time"] if v["graph_trusted"] else v["time"]
     peaks, peaks_src = load_peaks()
     hbm = peaks["hbm_gbs"]
     bf16 = peaks["bf16_tflops"]
@@ -559,27 +718,44 @@ def main():
     if prefill:
         # FP8 operands: measured BF16 peak x the nominal FP8/BF16 ratio (4.5 / 2.25)
         peak = bf16 * 2.0 if W.lins[0].qtype == "e4m3" else bf16
-        roof = {"bound": "tensor", "achieved": d["flops"] / d["time"] / 1e12, "peak": peak, "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": d["flops"] / d["launch_time"] / 1e12, "peak": peak,
+                "unit": "TFLOP/s",
+                "achieved_event_bracketed": d["flops"] / d["time"] / 1e12}
     else:
-        roof = {"bound": "hbm", "achieved": d["bytes"] / d["time"] / 1e9, "peak": hbm, "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": d["bytes"] / d["launch_time"] / 1e9, "peak": hbm, "unit": "GB/s",
+                "achieved_event_bracketed": d["bytes"] / d["time"] / 1e9}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["launch_us"] = d["launch_time"] / d["calls"] * 1e6
+    roof["launches_per_step"] = d["calls"]
     tr = traffic_for(dom.split("+")[-1], wl)
     roof["traffic"] = tr
     roof["kernel"] = dom
     roof["peak_source"] = f"{peaks_src} (MEASURED_PEAKS.json)" if peaks_src == "measured" else "fallback"
-    roof["timing"] = timing
+    roof["timing"] = (("per-launch duration = CUDA-event time of a graph holding only this kernel's calls "
+                       "of a step, back to back (alternating weight copies, more bytes than L2), / launches"
+                       if d["graph_trusted"] else
+                       f"per-launch duration from {timing} (this kernel's calls of a step fit in L2, so "
+                       "back-to-back replays of them alone would be served from L2)")
+                      + f"; 'achieved_event_bracketed' divides by the sum of {timing} (adds each launch's "
+                      "un-overlapped prologue and the event gaps)")
+    roof["kernels"] = {k: {"launches_per_step": v["calls"], "us_per_launch": round(v["launch_time"] / v["calls"] * 1e6, 2),
+                           "isolated_graph": v["graph_trusted"],
+                           "us_per_launch_event_bracketed": round(v["time"] / v["calls"] * 1e6, 2),
+                           "share_of_step": round(v["launch_time"] / sum(x["launch_time"] for x in per_kernel.values()), 3),
+                           "GB/s": round(v["bytes"] / v["launch_time"] / 1e9, 1),
+                           "TFLOP/s": round(v["flops"] / v["launch_time"] / 1e12, 1)}
+                       for k, v in per_kernel.items()}
     # roofline time over the whole step: sum_i max(bytes_i / BW, flops_i / peak_i) / measured
     rt = 0.0
-    for l in W.lins:
-        tpk = (bf16 * 2.0 if (l.form == "w8a8" and l.qtype == "e4m3") else bf16) * 1e12
-        rt += max(alg_bytes(l) / (hbm * 1e9), alg_flops(l) / tpk)
+    for i in range(n):
+        tpk = (bf16 * 2.0 if W.call_fp8[i] else bf16) * 1e12
+        rt += max(W.call_bytes[i] / (hbm * 1e9), W.call_flops[i] / tpk)
     roof["step_roofline_time_frac"] = rt / (mean_call.sum())
     calls = []
-    for i, l in enumerate(W.lins):
-        calls.append({"name": l.name, "M": l.M, "K": l.K, "N": l.N, "kernel": W.kernel[i],
-                      "us": round(mean_call[i] * 1e6, 2),
-                      "GB/s": round(alg_bytes(l) / mean_call[i] / 1e9, 1),
-                      "TFLOP/s": round(alg_flops(l) / mean_call[i] / 1e12, 1)})
+    for i in range(n):
+        calls.append(dict(W.call_info[i], kernel=W.kernel[i], us=round(mean_call[i] * 1e6, 2),
+                          **{"GB/s": round(W.call_bytes[i] / mean_call[i] / 1e9, 1),
+                             "TFLOP/s": round(W.call_flops[i] / mean_call[i] / 1e12, 1)}))
 
     # ---- end-to-end through the C ABI with host buffers ----
     e2e = None
@@ -596,9 +772,9 @@ def main():
         torch.cuda.synchronize()
         et = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
         e2e = {"value": whole_job_value(units_step, a.steps, world, et, unit_scale), "unit": metric_unit,
-               "h2d_bytes_per_step": int(sum(2 * l.M * l.K for l in W.lins)),
-               "d2h_bytes_per_step": int(sum(2 * l.M * l.N for l in W.lins)),
-               "how": "CUDA-graph replay: pinned-host activations copied in, the linears, outputs copied out"}
+               "h2d_bytes_per_step": int(sum(src.numel() * src.element_size() for _, src in W.h2d)),
+               "d2h_bytes_per_step": int(sum(src.numel() * src.element_size() for _, src in W.d2h)),
+               "how": "CUDA-graph replay: pinned-host inputs copied in, the step's kernels, outputs copied out"}
 
     stream_ctx.__exit__(None, None, None)
     cpu = None
@@ -610,15 +786,12 @@ def main():
             "metric": metric, "value": value, "unit": metric_unit, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("e4m3" if W.lins[0].qtype == "e4m3" else "int8") + ("xbf16" if W.lins[0].form == "w8a16" else "")
-                     + "->f32acc->bf16",
+            "dtype": W.dtype,
             "data": "synthetic",
-            "config": {"workload": wl, "linears": n, "bytes_per_step": bytes_step, "flops_per_step": flops_step,
-                       "weight_bytes": W.weight_bytes, "weight_copies": W.copies,
-                       "l2": (f"{W.copies} alternating weight copies of {W.weight_bytes / 1e6:.0f} MB each "
-                              f"(L2 is {L2_BYTES / 2**20:.0f} MiB)"),
-                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                       "timing": "CUDA-graph replay of whole steps, CUDA events around the K steps"},
+            "config": dict({"workload": wl, "bytes_per_step": bytes_step, "flops_per_step": flops_step},
+                           **W.extra_config,
+                           parallelism=f"replicas{world}" if world > 1 else "single-gpu",
+                           timing="CUDA-graph replay of whole steps, CUDA events around the K steps"),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,

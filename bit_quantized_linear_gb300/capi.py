@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libqlin.so")
 QLIN_OK, QLIN_ERR_INVALID_ARG, QLIN_ERR_UNSUPPORTED, QLIN_ERR_WORKSPACE, QLIN_ERR_CUDA, QLIN_ERR_TIMEOUT = range(6)
 QLIN_INT8, QLIN_E4M3 = 0, 1
 (QLIN_OP_QUANTIZE_WEIGHT, QLIN_OP_ACT_SCALE, QLIN_OP_QUANTIZE_ACT, QLIN_OP_W8A16_LINEAR,
- QLIN_OP_W8A8_LINEAR, QLIN_OP_I8_GEMM_S32, QLIN_OP_W8A8_DYNAMIC_LINEAR) = range(7)
+ QLIN_OP_W8A8_LINEAR, QLIN_OP_I8_GEMM_S32, QLIN_OP_W8A8_DYNAMIC_LINEAR, QLIN_OP_KV_STORE_MIXED,
+ QLIN_OP_KV_LOAD_MIXED) = range(9)
 
 QTYPES = {"int8": QLIN_INT8, "e4m3": QLIN_E4M3}
 
@@ -28,7 +29,8 @@ EXPORTS = ["qlin_quantize_weight", "qlin_act_scale_from_calib", "qlin_quantize_a
            "qlin_w8a16_linear", "qlin_w8a8_linear", "qlin_i8_gemm_s32", "qlin_workspace_bytes",
            "qlin_get_device_status", "qlin_status_string", "qlin_version", "qlin_debug_wait_flag",
            "qlin_kernel_name", "qlin_launch_count", "qlin_w8a8_linear_noalloc",
-           "qlin_quantize_act_dynamic", "qlin_w8a8_dynamic_linear"]
+           "qlin_quantize_act_dynamic", "qlin_w8a8_dynamic_linear", "qlin_kv_store_mixed",
+           "qlin_kv_load_mixed"]
 
 # Size of the library-owned scratch of qlin_w8a8_linear_noalloc (QLIN_W8A8_NOALLOC_SCRATCH_BYTES).
 W8A8_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -62,6 +64,8 @@ def _load() -> ctypes.CDLL:
         "qlin_w8a8_linear_noalloc": [I, I64, I64, I64, P, P, P, P, P, P, P],
         "qlin_quantize_act_dynamic": [I, I64, I64, P, P, P, P],
         "qlin_w8a8_dynamic_linear": [I, I64, I64, I64, P, P, P, P, P, P, SZ, P],
+        "qlin_kv_store_mixed": [I64, I64, I64, P, I64, P, I64, P, I64, P, P, P, P, P],
+        "qlin_kv_load_mixed": [I64, I64, I64, P, I64, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -178,6 +182,25 @@ def qlin_i8_gemm_s32(qx, qw, acc, ws=None, stream=None):
            "qlin_i8_gemm_s32")
 
 
+def qlin_kv_store_mixed(k, v, slots, k_cache, k_scale, v_cache, v_scale, stream=None):
+    """k, v: BF16 [T, ld] (row stride ld elements, last dim contiguous); slots int64 [T];
+    caches as allocated by kv_cache_alloc()."""
+    S, H, D = k_cache.shape
+    T = slots.shape[0]
+    assert k.stride(-1) == 1 and v.stride(-1) == 1
+    ldk = k.stride(0) if T > 0 else H * D
+    ldv = v.stride(0) if T > 0 else H * D
+    _check(_lib.qlin_kv_store_mixed(T, H, D, _p(k), ldk, _p(v), ldv, _p(slots), S, _p(k_cache), _p(k_scale),
+                                    _p(v_cache), _p(v_scale), _stream(stream)), "qlin_kv_store_mixed")
+
+
+def qlin_kv_load_mixed(slots, k_cache, k_scale, v_cache, v_scale, k_out, v_out, stream=None):
+    S, H, D = k_cache.shape
+    T = slots.shape[0]
+    _check(_lib.qlin_kv_load_mixed(T, H, D, _p(slots), S, _p(k_cache), _p(k_scale), _p(v_cache), _p(v_scale),
+                                   _p(k_out), _p(v_out), _stream(stream)), "qlin_kv_load_mixed")
+
+
 def qlin_kernel_name(op: int, qtype, M: int, K: int, N: int) -> str:
     return _lib.qlin_kernel_name(op, _qt(qtype), M, K, N).decode()
 
@@ -267,3 +290,23 @@ def i8_gemm_s32(qx, qw):
     ws = workspace(QLIN_OP_I8_GEMM_S32, QLIN_INT8, M, K, N, device=qx.device)
     qlin_i8_gemm_s32(qx, qw, acc, ws)
     return acc
+
+
+def kv_cache_alloc(num_slots: int, H: int, D: int, device=None):
+    """Device arrays of a mixed KV cache: k_cache int8 [S,H,D], k_scale float16 bits
+    [S,H,D/32] (int16 storage), v_cache E4M3 codes [S,H,D] (uint8), v_scale float16
+    bits [S,H] (int16 storage)."""
+    dev = device or "cuda"
+    return (torch.empty((num_slots, H, D), dtype=torch.int8, device=dev),
+            torch.empty((num_slots, H, D // 32), dtype=torch.int16, device=dev),
+            torch.empty((num_slots, H, D), dtype=torch.uint8, device=dev),
+            torch.empty((num_slots, H), dtype=torch.int16, device=dev))
+
+
+def kv_load_mixed(slots, cache):
+    S, H, D = cache[0].shape
+    T = slots.shape[0]
+    k = torch.empty((T, H, D), dtype=torch.bfloat16, device=slots.device)
+    v = torch.empty((T, H, D), dtype=torch.bfloat16, device=slots.device)
+    qlin_kv_load_mixed(slots, *cache, k, v)
+    return k, v

@@ -74,6 +74,20 @@ struct GemmArgs {
   int x_scale_per_token = 0;  // x_scale holds one scale per token row (dynamic W8A8)
 };
 
+// Mixed KV cache (kv_kernels.cu): INT8 keys with float16 group-32 scales,
+// E4M3 values with float16 per-(token, head) scales.
+struct KvArgs {
+  int64_t T, H, D;        // tokens, kv heads, head_dim (32, 64, 128 or 256)
+  const void *k, *v;      // BF16 rows of the new tokens (store), row strides ldk / ldv elements
+  int64_t ldk, ldv;
+  const int64_t *slots;   // [T] cache slot of each token; negative = padding
+  int64_t num_slots;
+  void *k_cache, *k_scale, *v_cache, *v_scale;  // [S,H,D] int8, [S,H,D/32] f16, [S,H,D] e4m3, [S,H] f16
+  void *k_out, *v_out;    // BF16 [T,H,D] (load)
+};
+cudaError_t launch_kv_store(const KvArgs &a, unsigned *status, int sms, cudaStream_t st);
+cudaError_t launch_kv_load(const KvArgs &a, unsigned *status, cudaStream_t st);
+
 cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 
 // tcgen05 kernels (gemm_tc.cu)

@@ -95,6 +95,18 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
       const int b = i8_swap_bnt(M);
       return names[b == 16 ? 0 : b == 32 ? 1 : 2];
     }
+    case QLIN_OP_KV_STORE_MIXED:
+    case QLIN_OP_KV_LOAD_MIXED: {
+      // M = tokens, K = head_dim, N = kv heads
+      if (M < 0 || N < 1 || !(K == 32 || K == 64 || K == 128 || K == 256)) return "invalid";
+      if (M == 0) return "none";
+      static const char *st[4] = {"k_kv_store_mixed<32>", "k_kv_store_mixed<64>", "k_kv_store_mixed<128>",
+                                  "k_kv_store_mixed<256>"};
+      static const char *ld[4] = {"k_kv_load_mixed<32>", "k_kv_load_mixed<64>", "k_kv_load_mixed<128>",
+                                  "k_kv_load_mixed<256>"};
+      const int i = K == 32 ? 0 : K == 64 ? 1 : K == 128 ? 2 : 3;
+      return op == QLIN_OP_KV_STORE_MIXED ? st[i] : ld[i];
+    }
     case QLIN_OP_W8A8_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
@@ -134,6 +146,9 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     // per-token codes (as for the static path) followed by the per-token scales
     case QLIN_OP_W8A8_DYNAMIC_LINEAR:
       return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256) + round_up((size_t)M * 4, 256);
+    case QLIN_OP_KV_STORE_MIXED:
+    case QLIN_OP_KV_LOAD_MIXED:
+      return 0;
   }
   return (size_t)-1;
 }
@@ -263,6 +278,47 @@ qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, co
   if (launch_i8_to_bf16(M, K, qx, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
   GemmArgs g{kI8Raw, QLIN_INT8, M, K, N, ws, qw, nullptr, nullptr, nullptr, acc};
   return from_cuda(launch_i8_swap(g, ws, true, *dev, st));
+}
+
+// Shared argument checks of the two KV-cache entry points.
+static qlin_status check_kv(int64_t T, int64_t H, int64_t D, const int64_t *slots, int64_t num_slots,
+                            const void *k_cache, const void *k_scale, const void *v_cache, const void *v_scale) {
+  if (T < 0 || H < 1 || num_slots < 0) return QLIN_ERR_INVALID_ARG;
+  if (!(D == 32 || D == 64 || D == 128 || D == 256)) return QLIN_ERR_INVALID_ARG;
+  if (H > 4096 || T > ((int64_t)1 << 40) / H || num_slots > ((int64_t)1 << 40) / H) return QLIN_ERR_INVALID_ARG;
+  if (T == 0) return QLIN_OK;
+  if (!slots || !al16(slots)) return QLIN_ERR_INVALID_ARG;
+  if (!k_cache || !k_scale || !v_cache || !v_scale) return QLIN_ERR_INVALID_ARG;
+  if (!al16(k_cache) || !al16(k_scale) || !al16(v_cache) || !al16(v_scale)) return QLIN_ERR_INVALID_ARG;
+  return QLIN_OK;
+}
+
+qlin_status qlin_kv_store_mixed(int64_t T, int64_t H, int64_t D, const void *k, int64_t ldk, const void *v,
+                                int64_t ldv, const int64_t *slots, int64_t num_slots, void *k_cache,
+                                void *k_scale, void *v_cache, void *v_scale, qlin_stream_t stream) {
+  if (qlin_status s = check_kv(T, H, D, slots, num_slots, k_cache, k_scale, v_cache, v_scale)) return s;
+  if (T > 0) {
+    if (!k || !v || !al16(k) || !al16(v)) return QLIN_ERR_INVALID_ARG;
+    if (ldk < H * D || ldv < H * D || (ldk % 8) || (ldv % 8)) return QLIN_ERR_INVALID_ARG;
+  }
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (T == 0) return QLIN_OK;
+  KvArgs a{T, H, D, k, v, ldk, ldv, slots, num_slots, k_cache, k_scale, v_cache, v_scale, nullptr, nullptr};
+  return from_cuda(launch_kv_store(a, dev->status, dev->sms, (cudaStream_t)stream));
+}
+
+qlin_status qlin_kv_load_mixed(int64_t T, int64_t H, int64_t D, const int64_t *slots, int64_t num_slots,
+                               const void *k_cache, const void *k_scale, const void *v_cache,
+                               const void *v_scale, void *k_out, void *v_out, qlin_stream_t stream) {
+  if (qlin_status s = check_kv(T, H, D, slots, num_slots, k_cache, k_scale, v_cache, v_scale)) return s;
+  if (T > 0 && (!k_out || !v_out || !al16(k_out) || !al16(v_out))) return QLIN_ERR_INVALID_ARG;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (T == 0) return QLIN_OK;
+  KvArgs a{T, H, D, nullptr, nullptr, 0, 0, slots, num_slots, (void *)k_cache, (void *)k_scale,
+           (void *)v_cache, (void *)v_scale, k_out, v_out};
+  return from_cuda(launch_kv_load(a, dev->status, (cudaStream_t)stream));
 }
 
 qlin_status qlin_get_device_status(qlin_stream_t stream) {

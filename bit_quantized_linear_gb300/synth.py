@@ -174,3 +174,42 @@ def make_inputs(lin: Linear, want=("w", "x", "cal", "bias"), x_rows: int | None 
     if "bias" in want and lin.bias:
         out["bias"] = bias(lin.N, rng_for(wl, L, f"{lin.name}.N{lin.N}", "bias"))
     return out
+
+
+# --------------------------------------------------------------------------
+# Mixed KV-cache workload: Qwen2.5-7B attention KV (28 layers, 4 kv heads,
+# head_dim 128) in a paged cache of 256-token blocks.  One step per layer:
+# an 8192-token prefill chunk is quantized into freshly allocated blocks, and
+# the layer's whole 32768-token context is read back as BF16 (the attention
+# read).  Block ids come from a seeded permutation (a block allocator hands out
+# non-contiguous blocks; tokens are contiguous inside a block).
+# --------------------------------------------------------------------------
+KV7B = "kv-mixed-7b"
+KV_LAYERS, KV_HEADS, KV_HEAD_DIM, KV_BLOCK = 28, 4, 128, 256
+KV_CHUNK, KV_CONTEXT = 8192, 32768
+
+
+def kv_block_table(layer: int, n_blocks: int = KV_CONTEXT // KV_BLOCK) -> np.ndarray:
+    return rng_for(KV7B, layer, "block_table", "perm").permutation(n_blocks)
+
+
+def kv_slots(blocks: np.ndarray, block: int = KV_BLOCK) -> np.ndarray:
+    """int64 slots of the tokens of the given blocks, in order."""
+    return (np.asarray(blocks, np.int64)[:, None] * block + np.arange(block, dtype=np.int64)[None, :]).reshape(-1)
+
+
+def kv_chunk_slots(layer: int) -> np.ndarray:
+    """Slots of the layer's prefill chunk: the first KV_CHUNK/KV_BLOCK blocks of its table."""
+    return kv_slots(kv_block_table(layer)[:KV_CHUNK // KV_BLOCK])
+
+
+def kv_context_slots(layer: int) -> np.ndarray:
+    """Slots of the layer's whole context, in block-table order."""
+    return kv_slots(kv_block_table(layer))
+
+
+def kv_tokens(layer: int, T: int, role: str) -> np.ndarray:
+    """BF16 bits [T, H*D] of new key or value rows, N(0,1) with 1% outlier channels x20."""
+    rng = rng_for(KV7B, layer, f"{role}.T{T}", "act")
+    outl = outlier_channels(KV_HEADS * KV_HEAD_DIM, rng_for(KV7B, layer, role, "outliers"))
+    return activations(T, KV_HEADS * KV_HEAD_DIM, rng, outl)

@@ -72,7 +72,9 @@ typedef enum {
   QLIN_OP_W8A16_LINEAR = 3,
   QLIN_OP_W8A8_LINEAR = 4,
   QLIN_OP_I8_GEMM_S32 = 5,
-  QLIN_OP_W8A8_DYNAMIC_LINEAR = 6
+  QLIN_OP_W8A8_DYNAMIC_LINEAR = 6,
+  QLIN_OP_KV_STORE_MIXED = 7, /* for qlin_kernel_name: M = tokens, K = head_dim, N = kv heads */
+  QLIN_OP_KV_LOAD_MIXED = 8
 } qlin_op;
 
 /*
@@ -222,13 +224,58 @@ qlin_status qlin_w8a8_linear_noalloc(qlin_qtype qtype, int64_t M, int64_t K, int
                                      const float *input_scale, const void *qw, const float *w_scale,
                                      const void *bias, void *y, qlin_stream_t stream);
 
+/*
+ * Mixed KV-cache quantization ("Nano-vLLM-MoE" README, section "KV cache
+ * compression": mixed K int8 + V FP8, K group 32, float16 scales; Highlights:
+ * dynamic per-token quantization; the layout below is the one whose size is
+ * the printed 0.5195x BF16 bytes per block).  A cache of num_slots slots (a
+ * slot is block * block_size + offset in a paged cache), H kv heads and
+ * head_dim D in {32, 64, 128, 256}, four device arrays the caller owns:
+ *   k_cache [num_slots, H, D]     int8 codes
+ *   k_scale [num_slots, H, D/32]  float16 bits, one per 32 consecutive elements
+ *   v_cache [num_slots, H, D]     E4M3 codes
+ *   v_scale [num_slots, H]        float16 bits, one per (slot, head)
+ *
+ * qlin_kv_store_mixed quantizes the T new tokens and writes them to their
+ * slots.  For token t with slot = slots[t] >= 0 and each head h:
+ *   key group g (elements 32g..32g+31):
+ *     s = RN_fp16(fl32(max|k| / 127)), saturating at 65504; 1.0 if that is 0
+ *     k_cache = clamp(rint(fl32(k / s)), -127, 127)   (round half to even)
+ *   value head:
+ *     s = RN_fp16(fl32(max|v| / 448)), same rules
+ *     v_cache = saturating RNE E4M3 cast of fl32(v / s)
+ *   k, v: BF16 [T, ld] device rows; token t's H*D elements (head-major) start
+ *     at k + t*ldk (v + t*ldv); ldk, ldv >= H*D and multiples of 8, so the key
+ *     and value columns of a fused QKV output can be passed in place.
+ *   slots: int64 [T] device array.  A negative slot skips the token (padding).
+ *     A slot >= num_slots breaks the contract: the token is skipped and the
+ *     device status word is set to QLIN_ERR_INVALID_ARG (reported by
+ *     qlin_get_device_status).  Two tokens with the same slot race.
+ *
+ * qlin_kv_load_mixed reads slots back as BF16 rows for attention:
+ *   k_out, v_out [T, H, D] BF16: RN_bf16(code * scale) (the product is exact
+ *   in fp32); a negative slot gives a row of +0; a slot >= num_slots gives +0
+ *   and sets the device status word to QLIN_ERR_INVALID_ARG.
+ *
+ * Both: T == 0 enqueues nothing; all pointers 16-byte aligned device pointers;
+ * no workspace.
+ */
+qlin_status qlin_kv_store_mixed(int64_t T, int64_t H, int64_t D, const void *k, int64_t ldk, const void *v,
+                                int64_t ldv, const int64_t *slots, int64_t num_slots, void *k_cache,
+                                void *k_scale, void *v_cache, void *v_scale, qlin_stream_t stream);
+qlin_status qlin_kv_load_mixed(int64_t T, int64_t H, int64_t D, const int64_t *slots, int64_t num_slots,
+                               const void *k_cache, const void *k_scale, const void *v_cache,
+                               const void *v_scale, void *k_out, void *v_out, qlin_stream_t stream);
+
 /* Workspace bytes an operation needs for these sizes (0 if none).  Returns
  * (size_t)-1 for invalid arguments. */
 size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, int64_t N);
 
 /* Synchronizes `stream`, then reports and clears the device status word of the
  * current device: QLIN_OK, or QLIN_ERR_TIMEOUT if a bounded device-side wait ran
- * out since the last call, or QLIN_ERR_CUDA if the stream reported an error. */
+ * out since the last call, QLIN_ERR_INVALID_ARG if a KV-cache kernel met a slot
+ * beyond the cache, or QLIN_ERR_CUDA if the stream reported an error.  The
+ * first error recorded since the last call wins. */
 qlin_status qlin_get_device_status(qlin_stream_t stream);
 
 /* Static, human-readable name of a status code. */

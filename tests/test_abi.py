@@ -78,6 +78,23 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert L.qlin_i8_gemm_s32(4, 64, 64, good, good, None, None, 0, None) == INV
     assert L.qlin_i8_gemm_s32(4, 64, 64, good, None, good, None, 0, None) == INV
     assert L.qlin_debug_wait_flag(None, 1000, None) == INV
+    # KV cache: head_dim outside {32,64,128,256}, bad strides, NULL / misaligned pointers
+    kv_store = lambda T, H, D, k, ldk, ldv, sl, kc: L.qlin_kv_store_mixed(T, H, D, k, ldk, good, ldv, sl, 64, kc,
+                                                                          good, good, good, None)
+    assert kv_store(4, 2, 96, good, 192, 192, good, good) == INV
+    assert kv_store(4, 2, 128, good, 200, 256, good, good) == INV  # ldk not a multiple of 8
+    assert kv_store(4, 2, 128, good, 248, 256, good, good) == INV  # ldk < H*D
+    assert kv_store(4, 2, 128, None, 256, 256, good, good) == INV
+    assert kv_store(4, 2, 128, odd, 256, 256, good, good) == INV
+    assert kv_store(4, 2, 128, good, 256, 256, None, good) == INV
+    assert kv_store(4, 0, 128, good, 256, 256, good, good) == INV
+    assert kv_store(-1, 2, 128, good, 256, 256, good, good) == INV
+    assert L.qlin_kv_load_mixed(4, 2, 128, good, 64, good, good, good, good, None, good, None) == INV
+    assert L.qlin_kv_load_mixed(4, 2, 128, good, 64, good, odd, good, good, good, good, None) == INV
+    assert L.qlin_kv_load_mixed(4, 2, 48, good, 64, good, good, good, good, good, good, None) == INV
+    assert capi.qlin_kernel_name(capi.QLIN_OP_KV_STORE_MIXED, 0, 8, 128, 4) == "k_kv_store_mixed<128>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_KV_LOAD_MIXED, 0, 8, 64, 4) == "k_kv_load_mixed<64>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_KV_LOAD_MIXED, 0, 8, 80, 4) == "invalid"
 
 
 def test_no_device_is_reported_not_crashed(capi):
