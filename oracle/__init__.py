@@ -5,7 +5,8 @@ quantized linear layer: per-output-channel weight quantizers (INT8 and OCP
 E4M3), the static activation scale from a calibration batch, static activation
 quantization, the exact INT8 accumulator, the fp64 W8A8 / W8A16 references and
 the mixed KV-cache quantizers (INT8 keys with float16 group scales, E4M3 values
-with float16 per-token scales).
+with float16 per-token scales) and the merged gate_up linear with the SiLU * up
+epilogue.
 The C source ``qlin_oracle.c`` cites the passages it follows.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
@@ -79,6 +80,10 @@ def lib() -> ctypes.CDLL:
             L.orc_kv_store.restype = I64
             L.orc_kv_load.argtypes = [I64, I64, I64, P, I64, P, P, P, P, P, P]
             L.orc_kv_load.restype = I64
+            L.orc_w8a16_gate_up_silu.argtypes = [I, I64, I64, I64, P, P, P, P, P, I64, P]
+            L.orc_w8a16_gate_up_silu.restype = I
+            L.orc_w8a8_gate_up_silu.argtypes = [I, I64, I64, I64, P, ctypes.c_float, P, P, P, P, I64, P]
+            L.orc_w8a8_gate_up_silu.restype = I
             L.orc_num_threads.argtypes = []
             L.orc_num_threads.restype = I
             _lib = L
@@ -202,6 +207,39 @@ def w8a8_per_token(qtype: int, qx, s_x, qw, s_w, bias=None, rows=None) -> np.nda
     y = np.empty((R, N), np.float64)
     lib().orc_w8a8_per_token(qtype, M, K, N, _ptr(qx), _ptr(s_x), _ptr(qw), _ptr(s_w), _ptr(b), _ptr(r), R,
                              _ptr(y))
+    return y
+
+
+def w8a16_gate_up_silu(qtype: int, x_bf16, qw, s_w, bias=None, rows=None) -> np.ndarray:
+    """fp64 silu(gate) * up of a merged gate_up W8A16 linear: qw [2I, K] (gate rows
+    first), s_w [2I], bias [2I] or None -> y [rows or M, I]."""
+    x = _c(x_bf16, np.uint16)
+    qw = _c(qw, np.uint8)
+    s_w = _c(s_w, np.float32)
+    M, K = x.shape
+    assert qw.shape[0] % 2 == 0
+    I = qw.shape[0] // 2
+    b = None if bias is None else _c(bias, np.uint16)
+    r, R = _rows(rows, M)
+    y = np.empty((R, I), np.float64)
+    if lib().orc_w8a16_gate_up_silu(qtype, M, K, I, _ptr(x), _ptr(qw), _ptr(s_w), _ptr(b), _ptr(r), R, _ptr(y)):
+        raise MemoryError("oracle temporary")
+    return y
+
+
+def w8a8_gate_up_silu(qtype: int, qx, s_x, qw, s_w, bias=None, rows=None) -> np.ndarray:
+    """fp64 silu(gate) * up of a merged gate_up W8A8 static linear."""
+    qx = _c(qx, np.uint8)
+    qw = _c(qw, np.uint8)
+    s_w = _c(s_w, np.float32)
+    M, K = qx.shape
+    I = qw.shape[0] // 2
+    b = None if bias is None else _c(bias, np.uint16)
+    r, R = _rows(rows, M)
+    y = np.empty((R, I), np.float64)
+    if lib().orc_w8a8_gate_up_silu(qtype, M, K, I, _ptr(qx), ctypes.c_float(float(np.float32(s_x))), _ptr(qw),
+                                   _ptr(s_w), _ptr(b), _ptr(r), R, _ptr(y)):
+        raise MemoryError("oracle temporary")
     return y
 
 

@@ -46,6 +46,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORC_INT8 0
@@ -264,6 +265,48 @@ void orc_w8a8_per_token(int qtype, int64_t M, int64_t K, int64_t N, const uint8_
       if (bias) v += (double)bf16_to_f32(bias[n]);
       y[i * N + n] = v;
     }
+}
+
+/* ---- merged gate_up linear with the SiLU * up epilogue -------------------
+ * The "tiny-vLLM" README's quality check quantizes 112 target layers of the
+ * 28-layer model, four linears per layer: merged qkv, o, merged gate_up, down.
+ * The MLP of that model family is down(silu(gate(x)) * up(x)) with the merged
+ * weight qw [2I, K] holding the gate rows [0, I) above the up rows [I, 2I).
+ * Reading: the fused epilogue applies the activation to the linear's exact
+ * outputs (no BF16 rounding of gate or up in between):
+ *   y[m, n] = silu(g) * u,  g = lin[m, n],  u = lin[m, I + n],
+ *   silu(g) = g / (1 + exp(-g)),  all in fp64;
+ * lin is the W8A16 or W8A8 reference above over N = 2I channels, with the
+ * optional bias [2I] added before the activation. */
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+static void glu_combine(int64_t R, int64_t I, const double *lin, double *y) {
+  for (int64_t i = 0; i < R; ++i)
+    for (int64_t n = 0; n < I; ++n) y[i * I + n] = silu(lin[i * 2 * I + n]) * lin[i * 2 * I + I + n];
+}
+
+/* Returns 0 on success, -1 if the temporary [rows, 2I] buffer cannot be allocated. */
+int orc_w8a16_gate_up_silu(int qtype, int64_t M, int64_t K, int64_t I, const uint16_t *x, const uint8_t *qw,
+                           const float *s_w, const uint16_t *bias, const int64_t *rows, int64_t nrows, double *y) {
+  int64_t R = rows ? nrows : M;
+  double *lin = (double *)malloc((size_t)(R > 0 ? R : 1) * (size_t)(2 * I) * sizeof(double));
+  if (!lin) return -1;
+  orc_w8a16(qtype, M, K, 2 * I, x, qw, s_w, bias, rows, nrows, lin);
+  glu_combine(R, I, lin, y);
+  free(lin);
+  return 0;
+}
+
+int orc_w8a8_gate_up_silu(int qtype, int64_t M, int64_t K, int64_t I, const uint8_t *qx, float s_x,
+                          const uint8_t *qw, const float *s_w, const uint16_t *bias, const int64_t *rows,
+                          int64_t nrows, double *y) {
+  int64_t R = rows ? nrows : M;
+  double *lin = (double *)malloc((size_t)(R > 0 ? R : 1) * (size_t)(2 * I) * sizeof(double));
+  if (!lin) return -1;
+  orc_w8a8(qtype, M, K, 2 * I, qx, s_x, qw, s_w, bias, rows, nrows, lin);
+  glu_combine(R, I, lin, y);
+  free(lin);
+  return 0;
 }
 
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
