@@ -60,13 +60,21 @@ def workload_calls(name: str):
         return synth.stack_linears("decode"), synth.STACK + "-decode"
     if name == "stack-prefill":
         return synth.stack_linears("prefill"), synth.STACK + "-prefill"
+    if name == "stack-fused-decode":
+        return synth.stack_linears("decode", fused=True), synth.STACK + "-fused-decode"
+    if name == "stack-fused-prefill":
+        return synth.stack_linears("prefill", fused=True), synth.STACK + "-fused-prefill"
     if name == "kv7b":
         return [], synth.KV7B
     raise SystemExit(f"unknown workload {name}")
 
 
+def out_cols(l) -> int:
+    return l.N // 2 if l.glu else l.N
+
+
 def alg_bytes(l) -> int:
-    b = l.N * l.K + 4 * l.N + 2 * l.M * l.K + 2 * l.M * l.N
+    b = l.N * l.K + 4 * l.N + 2 * l.M * l.K + 2 * l.M * out_cols(l)
     if l.bias:
         b += 2 * l.N
     return b
@@ -77,7 +85,7 @@ def alg_flops(l) -> int:
 
 
 def is_prefill(name: str) -> bool:
-    return name in ("prefill", "stack-prefill")
+    return name in ("prefill", "stack-prefill", "stack-fused-prefill")
 
 
 def load_peaks():
@@ -202,23 +210,23 @@ class GpuWorkload:
                 if k not in cache:
                     cache[k] = synth.make_inputs(l, want=("x", "cal", "bias"))
                 t = cache[k]
-            shape_key = (l.form, l.qtype, l.M, l.K, l.N)
+            shape_key = (l.form, l.qtype, l.M, l.K, l.N, l.glu)
             if self.device_gen:
                 # the stack's 216 calls are sequential on one stream: outputs, scratch and
                 # pinned host staging are shared per shape (each layer keeps its own x)
                 xt = t["x_dev"]
                 if ("xh",) + shape_key not in shared:
                     shared[("xh",) + shape_key] = xt.cpu().pin_memory()
-                    shared[("y",) + shape_key] = torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev)
-                    shared[("yh",) + shape_key] = torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory()
+                    shared[("y",) + shape_key] = torch.empty((l.M, out_cols(l)), dtype=torch.bfloat16, device=dev)
+                    shared[("yh",) + shape_key] = torch.empty((l.M, out_cols(l)), dtype=torch.bfloat16).pin_memory()
                 self.x_host.append(shared[("xh",) + shape_key])
                 self.y.append(shared[("y",) + shape_key])
                 self.y_host.append(shared[("yh",) + shape_key])
             else:
                 xt = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
                 self.x_host.append(torch.from_numpy(t["x"].view(np.int16)).view(torch.bfloat16).pin_memory())
-                self.y.append(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev))
-                self.y_host.append(torch.empty((l.M, l.N), dtype=torch.bfloat16).pin_memory())
+                self.y.append(torch.empty((l.M, out_cols(l)), dtype=torch.bfloat16, device=dev))
+                self.y_host.append(torch.empty((l.M, out_cols(l)), dtype=torch.bfloat16).pin_memory())
             self.x.append(xt)
             self.bias.append(torch.from_numpy(t["bias"].view(np.int16)).to(dev).view(torch.bfloat16)
                              if "bias" in t else None)
@@ -234,8 +242,10 @@ class GpuWorkload:
             else:
                 self.sx.append(None)
                 op = capi.QLIN_OP_W8A16_LINEAR
+            if l.glu:
+                op = capi.QLIN_OP_W8A8_GATE_UP_SILU if l.form == "w8a8" else capi.QLIN_OP_W8A16_GATE_UP_SILU
             if ("ws",) + shape_key not in shared or not self.device_gen:
-                shared[("ws",) + shape_key] = capi.workspace(op, l.qtype, l.M, l.K, l.N, device=dev)
+                shared[("ws",) + shape_key] = capi.workspace(op, l.qtype, l.M, l.K, out_cols(l), device=dev)
             self.ws.append(shared[("ws",) + shape_key])
             if len(cache) > 8:
                 cache.clear()
@@ -258,14 +268,14 @@ class GpuWorkload:
                     self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.wsets[c][key]),
                                          ptr(self.scales[key]), ptr(self.bias[i]), ptr(self.y[i]), wsp, wsb, sp))
             elif l.form == "w8a16":
-                self.fns.append(L.qlin_w8a16_linear)
+                self.fns.append(L.qlin_w8a16_gate_up_silu if l.glu else L.qlin_w8a16_linear)
                 for c in range(self.copies):
-                    self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.wsets[c][key]),
+                    self.args[c].append((qt, l.M, l.K, out_cols(l), ptr(self.x[i]), ptr(self.wsets[c][key]),
                                          ptr(self.scales[key]), ptr(self.bias[i]), ptr(self.y[i]), wsp, wsb, sp))
             else:
-                self.fns.append(L.qlin_w8a8_linear)
+                self.fns.append(L.qlin_w8a8_gate_up_silu if l.glu else L.qlin_w8a8_linear)
                 for c in range(self.copies):
-                    self.args[c].append((qt, l.M, l.K, l.N, ptr(self.x[i]), ptr(self.sx[i]),
+                    self.args[c].append((qt, l.M, l.K, out_cols(l), ptr(self.x[i]), ptr(self.sx[i]),
                                          ptr(self.wsets[c][key]), ptr(self.scales[key]), ptr(self.bias[i]),
                                          ptr(self.y[i]), wsp, wsb, sp))
         op = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR,
@@ -279,7 +289,8 @@ class GpuWorkload:
         self.call_bytes = [alg_bytes(l) for l in self.lins]
         self.call_flops = [alg_flops(l) for l in self.lins]
         self.call_fp8 = [l.form == "w8a8" and l.qtype == "e4m3" for l in self.lins]
-        self.call_info = [{"name": l.name, "M": l.M, "K": l.K, "N": l.N} for l in self.lins]
+        self.call_info = [{"name": l.name, "M": l.M, "K": l.K, "N": l.N, **({"out": out_cols(l)} if l.glu else {})}
+                          for l in self.lins]
         self.h2d = [(self.x[i], self.x_host[i]) for i in range(len(self.lins))]
         self.d2h = [(self.y_host[i], self.y[i]) for i in range(len(self.lins))]
         l0 = self.lins[0]
@@ -498,7 +509,7 @@ def oracle_sample(name, rows_per_call=1):
         return oracle_kv_sample()
     lins, wl = workload_calls(name)
     if name.startswith("stack"):
-        lins = lins[:6]  # one layer of the stack
+        lins = lins[:4 if "fused" in name else 6]  # one layer of the stack
     prepared = []
     for l in lins:
         t = synth.make_inputs(l, want=("w", "cal", "bias"))
@@ -508,12 +519,16 @@ def oracle_sample(name, rows_per_call=1):
         # the first r rows of the workload's activations (the generator draws rows in order)
         x = synth.make_inputs(l, want=("x",), x_rows=r)["x"]
         sx = oracle.act_scale(qt, t["cal"]) if l.form == "w8a8" and "cal" in t else None
-        sub = synth.Linear(l.name, l.K, l.N, r, l.qtype, l.form, l.bias, l.outliers, l.workload, l.layer)
+        sub = synth.Linear(l.name, l.K, l.N, r, l.qtype, l.form, l.bias, l.outliers, l.workload, l.layer, l.glu)
         prepared.append((l, sub, qt, q, s, x, sx, t.get("bias")))
 
     def run():
         for l, sub, qt, q, s, x, sx, b in prepared:
-            if l.form == "w8a16":
+            if l.glu and l.form == "w8a16":
+                oracle.w8a16_gate_up_silu(qt, x, q, s, b)
+            elif l.glu:
+                oracle.w8a8_gate_up_silu(qt, oracle.quantize_act(qt, x, sx), sx, q, s, b)
+            elif l.form == "w8a16":
                 oracle.w8a16(qt, x, q, s, b)
             elif l.form == "w8a8dyn":
                 qx, sxr = oracle.quantize_act_per_token(qt, x)
@@ -571,7 +586,7 @@ def main():
     ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
     ap.add_argument("--workload", default="decode7b",
                     choices=["decode7b", "small", "w8a8-3b", "w8a8-dyn-3b", "prefill", "stack-decode",
-                             "stack-prefill", "kv7b"])
+                             "stack-prefill", "stack-fused-decode", "stack-fused-prefill", "kv7b"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()

@@ -20,7 +20,7 @@ QLIN_OK, QLIN_ERR_INVALID_ARG, QLIN_ERR_UNSUPPORTED, QLIN_ERR_WORKSPACE, QLIN_ER
 QLIN_INT8, QLIN_E4M3 = 0, 1
 (QLIN_OP_QUANTIZE_WEIGHT, QLIN_OP_ACT_SCALE, QLIN_OP_QUANTIZE_ACT, QLIN_OP_W8A16_LINEAR,
  QLIN_OP_W8A8_LINEAR, QLIN_OP_I8_GEMM_S32, QLIN_OP_W8A8_DYNAMIC_LINEAR, QLIN_OP_KV_STORE_MIXED,
- QLIN_OP_KV_LOAD_MIXED) = range(9)
+ QLIN_OP_KV_LOAD_MIXED, QLIN_OP_W8A16_GATE_UP_SILU, QLIN_OP_W8A8_GATE_UP_SILU) = range(11)
 
 QTYPES = {"int8": QLIN_INT8, "e4m3": QLIN_E4M3}
 
@@ -30,7 +30,7 @@ EXPORTS = ["qlin_quantize_weight", "qlin_act_scale_from_calib", "qlin_quantize_a
            "qlin_get_device_status", "qlin_status_string", "qlin_version", "qlin_debug_wait_flag",
            "qlin_kernel_name", "qlin_launch_count", "qlin_w8a8_linear_noalloc",
            "qlin_quantize_act_dynamic", "qlin_w8a8_dynamic_linear", "qlin_kv_store_mixed",
-           "qlin_kv_load_mixed"]
+           "qlin_kv_load_mixed", "qlin_w8a16_gate_up_silu", "qlin_w8a8_gate_up_silu"]
 
 # Size of the library-owned scratch of qlin_w8a8_linear_noalloc (QLIN_W8A8_NOALLOC_SCRATCH_BYTES).
 W8A8_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
         "qlin_w8a8_dynamic_linear": [I, I64, I64, I64, P, P, P, P, P, P, SZ, P],
         "qlin_kv_store_mixed": [I64, I64, I64, P, I64, P, I64, P, I64, P, P, P, P, P],
         "qlin_kv_load_mixed": [I64, I64, I64, P, I64, P, P, P, P, P, P, P],
+        "qlin_w8a16_gate_up_silu": [I, I64, I64, I64, P, P, P, P, P, P, SZ, P],
+        "qlin_w8a8_gate_up_silu": [I, I64, I64, I64, P, P, P, P, P, P, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -180,6 +182,23 @@ def qlin_i8_gemm_s32(qx, qw, acc, ws=None, stream=None):
     wp, wb = _ws(ws)
     _check(_lib.qlin_i8_gemm_s32(M, K, N, _p(qx), _p(qw), _p(acc), wp, wb, _stream(stream)),
            "qlin_i8_gemm_s32")
+
+
+def qlin_w8a16_gate_up_silu(qtype, x, qw, w_scale, bias, y, ws=None, stream=None):
+    """qw [2I, K] (gate rows first), y [M, I]."""
+    M, K = x.shape
+    I = qw.shape[0] // 2
+    wp, wb = _ws(ws)
+    _check(_lib.qlin_w8a16_gate_up_silu(_qt(qtype), M, K, I, _p(x), _p(qw), _p(w_scale), _p(bias), _p(y), wp, wb,
+                                        _stream(stream)), "qlin_w8a16_gate_up_silu")
+
+
+def qlin_w8a8_gate_up_silu(qtype, x, input_scale, qw, w_scale, bias, y, ws, stream=None):
+    M, K = x.shape
+    I = qw.shape[0] // 2
+    wp, wb = _ws(ws)
+    _check(_lib.qlin_w8a8_gate_up_silu(_qt(qtype), M, K, I, _p(x), _p(input_scale), _p(qw), _p(w_scale), _p(bias),
+                                       _p(y), wp, wb, _stream(stream)), "qlin_w8a8_gate_up_silu")
 
 
 def qlin_kv_store_mixed(k, v, slots, k_cache, k_scale, v_cache, v_scale, stream=None):
@@ -310,3 +329,20 @@ def kv_load_mixed(slots, cache):
     v = torch.empty((T, H, D), dtype=torch.bfloat16, device=slots.device)
     qlin_kv_load_mixed(slots, *cache, k, v)
     return k, v
+
+
+def w8a16_gate_up_silu(qtype, x, qw, w_scale, bias=None):
+    M, K = x.shape
+    I = qw.shape[0] // 2
+    y = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    qlin_w8a16_gate_up_silu(qtype, x, qw, w_scale, bias, y)
+    return y
+
+
+def w8a8_gate_up_silu(qtype, x, input_scale, qw, w_scale, bias=None):
+    M, K = x.shape
+    I = qw.shape[0] // 2
+    y = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    ws = workspace(QLIN_OP_W8A8_GATE_UP_SILU, qtype, M, K, I, device=x.device)
+    qlin_w8a8_gate_up_silu(qtype, x, input_scale, qw, w_scale, bias, y, ws)
+    return y

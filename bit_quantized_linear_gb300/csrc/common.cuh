@@ -88,6 +88,13 @@ __device__ __forceinline__ float code_to_f32(uint8_t c) {
   }
 }
 
+// SiLU of the merged gate_up epilogue: g * sigmoid(g) = g / (1 + exp(-g)), with
+// CUDA's fast exponential and division intrinsics (relative error ~2^-21, far
+// below the BF16 rounding of the output).  Extremes: for g > ~88, exp(-g) is 0
+// and the result is g; for g < ~-87, 1 + exp(-g) exceeds 2^126 and __fdividef
+// returns 0, where the exact value is below 2^-100 in magnitude.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -81,9 +81,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // producer, 1 = TMEM allocator + MMA issuer, 4..11 = epilogue (two quads, each
 // owning 128 of the tile's 256 channels).
 struct Fp8Params {
-  int M, N, K;
+  int M, N, K;  // N: output channels (the intermediate size I when glu)
   int mtiles, ntiles;
   int xs_per_token;  // x_scale holds one scale per token row
+  int glu;           // merged gate_up: B tile = 128 gate rows + the matching 128 up rows
   const float *w_scale;
   const float *x_scale;
   const uint16_t *bias;
@@ -153,7 +154,12 @@ __global__ void __launch_bounds__(384, 1)
           uint8_t *st = smem + s * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           tma_load_2d(&tm_a, &full[s], st, kb * C::BK, m0);
-          tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, n0);
+          if (p.glu) {  // gate rows n0/2.. and the matching up rows N + n0/2.. (box of 128 rows each)
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, n0 / 2);
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, p.N + n0 / 2);
+          } else {
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, n0);
+          }
         }
       }
     }
@@ -211,6 +217,42 @@ __global__ void __launch_bounds__(384, 1)
       uint16_t *yrow = p.y + (size_t)m * p.N;
       // per-token activation scale multiplies the row (lane = token)
       const float sxm = p.xs_per_token ? (m < p.M ? __ldg(p.x_scale + m) : 0.0f) : 1.0f;
+      if (p.glu) {
+        // columns [0,128) hold gate channels n0/2 + c, columns [128,256) the matching up
+        // channels; half h takes gate columns [64h, 64h + 64) and their up partners
+        const int nb0 = n0 / 2;
+#pragma unroll 1
+        for (int c = 64 * half; c < 64 * half + 64; c += 32) {
+          uint32_t rg[32], ru[32];
+          tmem_ld32(tmem + lane_base + b * C::BN + c, rg);
+          tmem_ld32(tmem + lane_base + b * C::BN + 128 + c, ru);
+          const int nb = nb0 + c;
+          const float sg = sx * __ldg(p.w_scale + nb + lane), su = sx * __ldg(p.w_scale + p.N + nb + lane);
+          const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + nb + lane)) : 0.0f;
+          const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + nb + lane)) : 0.0f;
+          tmem_ld_wait();
+          uint32_t o[16];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            float v[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = 2 * h + e;
+              const float g = fmaf(__uint_as_float(rg[col]), sxm * __shfl_sync(0xffffffffu, sg, col),
+                                   __shfl_sync(0xffffffffu, bg, col));
+              const float u = fmaf(__uint_as_float(ru[col]), sxm * __shfl_sync(0xffffffffu, su, col),
+                                   __shfl_sync(0xffffffffu, bu, col));
+              v[e] = silu_f(g) * u;
+            }
+            o[h] = pack_bf16x2(v[0], v[1]);
+          }
+          if (m < p.M) {
+            uint4 *dst = reinterpret_cast<uint4 *>(yrow + nb);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int c = 128 * half; c < 128 * half + 128; c += 32) {
         uint32_t r[32];
@@ -236,6 +278,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int g = 0; g < 4; ++g)
             if (nb + 8 * g < p.N) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
         }
+      }
       }
       tc_fence_before();
       __syncwarp();
@@ -269,8 +312,9 @@ __global__ void __launch_bounds__(384, 1)
 enum SwapMode { kSwapW8A16 = 0, kSwapI8Scaled = 1, kSwapI8Raw = 2 };
 
 struct SwapParams {
-  int M, N, K;
+  int M, N, K;       // N: output channels (the intermediate size I when glu)
   int xs_per_token;  // x_scale holds one scale per token (I8 scaled mode)
+  int glu;           // merged gate_up: a 128-row tile = 64 gate rows + their 64 up rows
   int splits;        // CTAs per cluster along K (gridDim.z)
   int units;   // output tiles: n-tiles x token tiles
   int ntiles;  // n-tiles (128 channels each)
@@ -313,7 +357,10 @@ struct DqCfg {
   static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
   static constexpr int R = (R0 > 15 ? 15 : R0) / 3 * 3;  // raw stages
   static constexpr int X_OFF = 0, RAW_OFF = X * X_BYTES, BAR_OFF = RAW_OFF + R * RAW_BYTES;
-  static constexpr int SMEM = BAR_OFF + 1024 + 1024;  // alignment slack + barriers
+  // merged gate_up: per 16-token chunk the gate rows pass g of tokens 8..15 and the up
+  // rows u of tokens 0..7 to each other; two slots, so a side can run one chunk ahead
+  static constexpr int XCHG_OFF = BAR_OFF + 1024, XCHG_BYTES = 2 * 2 * 8 * 64 * 4;
+  static constexpr int SMEM = XCHG_OFF + XCHG_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
   static_assert(R % QUADS == 0 && R >= 6, "raw ring depth: multiple of the converter quads");
   static_assert(NA % (QUADS * ISSUERS) == 0, "A ring depth: multiple of quads x issuers");
@@ -321,7 +368,7 @@ struct DqCfg {
   static_assert(ND * DSTRIDE <= ACOL && ACOL + NA * 32 <= 512, "TMEM columns");
   static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(2 * (R + X + NA + ND) * 8 + 16 <= 1024, "barrier area");
+  static_assert(2 * (R + X + NA + ND + 4) * 8 + 16 <= 1024, "barrier area");
 };
 
 // 16 weight codes -> 16 exact BF16 values packed in 8 words (k order kept).
@@ -381,6 +428,27 @@ __device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const 
   }
 }
 
+// Merged gate_up (S > 1 path): 4 consecutive output channels of one token row
+// from the summed gate and up accumulators: y = silu(gate) * up.
+template <int MODE>
+__device__ __forceinline__ void glu_store4(const SwapParams &p, int m, int ch, const uint32_t (&g)[4],
+                                           const uint32_t (&u)[4]) {
+  const float sx = MODE == kSwapI8Scaled ? __ldg(p.x_scale + (p.xs_per_token ? m : 0)) : 1.0f;
+  float y[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float ga = MODE == kSwapW8A16 ? __uint_as_float(g[e]) : (float)(int)g[e];
+    const float ua = MODE == kSwapW8A16 ? __uint_as_float(u[e]) : (float)(int)u[e];
+    const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + ch + e)) : 0.0f;
+    const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + ch + e)) : 0.0f;
+    const float gv = fmaf(ga, sx * __ldg(p.w_scale + ch + e), bg);
+    const float uv = fmaf(ua, sx * __ldg(p.w_scale + p.N + ch + e), bu);
+    y[e] = silu_f(gv) * uv;
+  }
+  *reinterpret_cast<uint2 *>((uint16_t *)p.y + (size_t)m * p.N + ch) =
+      make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+}
+
 template <int BNT, int QT, int MODE>
 __global__ void __launch_bounds__(640, 1)
     k_w8_dq(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, SwapParams p) {
@@ -396,8 +464,12 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t *x_full = raw_empty + C::R, *x_empty = x_full + C::X;
   uint64_t *a_full = x_empty + C::X, *a_empty = a_full + C::NA;
   uint64_t *acc_full = a_empty + C::NA, *acc_empty = acc_full + C::ND;
-  uint32_t *tmem_slot = (uint32_t *)(acc_empty + C::ND);
+  // merged gate_up exchange, per slot: g_ready, u_ready (the writers' two warps arrive),
+  // g_taken, u_taken (the readers' two warps arrive)
+  uint64_t *g_ready = acc_empty + C::ND, *u_ready = g_ready + 2, *g_taken = u_ready + 2, *u_taken = g_taken + 2;
+  uint32_t *tmem_slot = (uint32_t *)(u_taken + 2);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+  float *xchg = reinterpret_cast<float *>(smem + C::XCHG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.z, S = p.splits;
   const int KB = (p.K + C::BK - 1) / C::BK;
@@ -411,8 +483,8 @@ __global__ void __launch_bounds__(640, 1)
   {  // barrier initialisation spread over the threads (one barrier each)
     const int t = threadIdx.x;
     constexpr int B0 = C::R, B1 = 2 * C::R, B2 = B1 + C::X, B3 = B2 + C::X, B4 = B3 + C::NA, B5 = B4 + C::NA,
-                  B6 = B5 + C::ND, B7 = B6 + C::ND;
-    static_assert(B7 < C::THREADS, "one thread per barrier");
+                  B6 = B5 + C::ND, B7 = B6 + C::ND, B8 = B7 + 8;
+    static_assert(B8 < C::THREADS, "one thread per barrier");
     uint64_t *bar = nullptr;
     uint32_t cnt = 1;
     if (t < B0) bar = &raw_full[t];
@@ -423,6 +495,7 @@ __global__ void __launch_bounds__(640, 1)
     else if (t < B5) bar = &a_empty[t - B4];
     else if (t < B6) bar = &acc_full[t - B5], cnt = C::ISSUERS;  // one commit per MMA issuer
     else if (t < B7) bar = &acc_empty[t - B6], cnt = 4;          // the epilogue quad
+    else if (t < B8) bar = &g_ready[t - B7], cnt = 2;            // exchange barriers: two warps each
     if (bar) {
       mbar_init(bar, cnt);
       fence_barrier_init();
@@ -445,7 +518,7 @@ __global__ void __launch_bounds__(640, 1)
     if (lane == 0) {
       int i = 0;
       for (int j = 0; j < my_units && !*abort_flag; ++j) {
-        const int n0 = ((blockIdx.x + j * G) % p.ntiles) * C::BM;
+        const int tt = (blockIdx.x + j * G) % p.ntiles;
         for (int kb = 0; kb < nkb; ++kb, ++i) {
           const int s = i % C::R;
           if (i >= C::R && !mbar_wait(&raw_empty[s], ((i / C::R) & 1) ^ 1, abort_flag)) {
@@ -453,7 +526,13 @@ __global__ void __launch_bounds__(640, 1)
             break;
           }
           mbar_arrive_expect_tx(&raw_full[s], C::RAW_BYTES);
-          tma_load_2d(&tm_w, &raw_full[s], raws + s * C::RAW_BYTES, (kb0 + kb) * C::BK, n0);
+          uint8_t *dst = raws + s * C::RAW_BYTES;
+          if (p.glu) {  // 64 gate rows, then their 64 up rows (the 64-byte swizzle repeats every 8 rows)
+            tma_load_2d(&tm_w, &raw_full[s], dst, (kb0 + kb) * C::BK, tt * 64);
+            tma_load_2d(&tm_w, &raw_full[s], dst + 64 * C::BK, (kb0 + kb) * C::BK, p.N + tt * 64);
+          } else {
+            tma_load_2d(&tm_w, &raw_full[s], dst, (kb0 + kb) * C::BK, tt * C::BM);
+          }
         }
       }
     }
@@ -561,17 +640,70 @@ __global__ void __launch_bounds__(640, 1)
   } else if (warp >= 16) {  // ------------------ epilogue quad
     const int q4 = warp & 3, nl = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    int cidx = 0;
+    const bool up_row = p.glu && nl >= 64;  // merged gate_up: TMEM lanes 64..127 hold the up rows
+    int cidx = 0, xround = 0;
     bool ok = true;
+    // Writes the outputs of this thread's row for tokens m0 + c .. m0 + c + 15 from
+    // their fp32 values (scale and bias applied).  Merged gate_up: gate row n and
+    // up row n are in different warps; the gate rows' threads hand g of tokens
+    // 8..15 to the up rows' threads and receive u of tokens 0..7, then each side
+    // stores silu(g) * u for its half of the tokens (shared-memory slots with
+    // mbarriers, bounded waits).  Returns false if a wait ran out.  All four
+    // warps call it equally often.
+    auto emit16 = [&](int m0, int c, int ochan, const float (&v)[16]) -> bool {
+      uint16_t *y = (uint16_t *)p.y;
+      if (!p.glu) {
+        if (ochan < p.N) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int m = m0 + c + e;
+            if (m < p.M) y[(size_t)m * p.N + ochan] = f32_to_bf16_bits(v[e]);
+          }
+        }
+        return true;
+      }
+      const int k = xround++, slot = k & 1, use = k >> 1;  // use: how often this slot was used before
+      const int col = nl & 63;
+      float *mine = xchg + (slot * 2 + (up_row ? 1 : 0)) * 8 * 64;  // gate: [slot][0], up: [slot][1]
+      float *theirs = xchg + (slot * 2 + (up_row ? 0 : 1)) * 8 * 64;
+      uint64_t *my_ready = (up_row ? u_ready : g_ready) + slot, *their_ready = (up_row ? g_ready : u_ready) + slot;
+      uint64_t *my_taken = (up_row ? u_taken : g_taken) + slot, *their_taken = (up_row ? g_taken : u_taken) + slot;
+      // 1. the other side has read what this side wrote into the slot last time
+      const bool w0 = use == 0 || mbar_wait(my_taken, (use - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w0)) return false;
+      // the up rows hand over tokens 0..7 and keep 8..15, the gate rows the other way
+      // round (selects between constant indices keep v[] in registers)
+      const int keep = up_row ? 8 : 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mine[e * 64 + col] = up_row ? v[e] : v[8 + e];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(my_ready);
+      // 2. the other side's values for the tokens this side stores
+      const bool w1 = mbar_wait(their_ready, use & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w1)) return false;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float other = theirs[e * 64 + col];
+        const float own = up_row ? v[8 + e] : v[e];
+        const float g = up_row ? other : own, u = up_row ? own : other;
+        const int m = m0 + c + keep + e;
+        if (m < p.M) y[(size_t)m * p.N + ochan] = f32_to_bf16_bits(silu_f(g) * u);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(their_taken);
+      return true;
+    };
     for (int j = 0; j < my_units && ok; ++j) {
       const int u = blockIdx.x + j * G;
-      const int n0 = (u % p.ntiles) * C::BM, m0 = (u / p.ntiles) * BNT;
-      const int n = n0 + nl;
-      const bool valid = n < p.N;
+      const int tt = u % p.ntiles, m0 = (u / p.ntiles) * BNT;
+      // weight row of this TMEM lane and the output channel it writes
+      const int wrow = !p.glu ? tt * C::BM + nl : (up_row ? p.N + tt * 64 + (nl - 64) : tt * 64 + nl);
+      const int ochan = p.glu ? tt * 64 + (nl & 63) : wrow;
+      const bool valid = p.glu ? true : wrow < p.N;
       int32_t sums[kI8 ? BNT : 1];
 #pragma unroll
       for (int c = 0; c < (kI8 ? BNT : 1); ++c) sums[c] = 0;
-      for (int ch = 0; ch < chunks_per_unit; ++ch, ++cidx) {
+      for (int ch = 0; ch < chunks_per_unit && ok; ++ch, ++cidx) {
         const int db = cidx % C::ND;
         ok = mbar_wait(&acc_full[db], (cidx / C::ND) & 1, abort_flag);
         tc_fence_after();
@@ -609,20 +741,16 @@ __global__ void __launch_bounds__(640, 1)
             }
           }
         } else if (S == 1) {
-          const float sw = valid ? __ldg(p.w_scale + n) : 0.0f;
-          const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
-          uint16_t *y = (uint16_t *)p.y;
+          const float sw = valid ? __ldg(p.w_scale + wrow) : 0.0f;
+          const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + wrow)) : 0.0f;
 #pragma unroll 1
-          for (int c = 0; c < BNT; c += 16) {
+          for (int c = 0; c < BNT && ok; c += 16) {
             uint32_t r[16];
             load16(c, r);
-            if (valid) {
+            float v[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int m = m0 + c + e;
-                if (m < p.M) y[(size_t)m * p.N + n] = f32_to_bf16_bits(fmaf(__uint_as_float(r[e]), sw, b));
-              }
-            }
+            for (int e = 0; e < 16; ++e) v[e] = fmaf(__uint_as_float(r[e]), sw, b);
+            ok = emit16(m0, c, ochan, v);
           }
         } else {
           uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // partial tile, [token][channel]
@@ -641,21 +769,28 @@ __global__ void __launch_bounds__(640, 1)
       if constexpr (kI8) {
         if (ok) {
           if (S == 1) {
-            if (valid) {
-              if constexpr (MODE == kSwapI8Raw) {
+            if constexpr (MODE == kSwapI8Raw) {
+              if (valid) {
 #pragma unroll
                 for (int c = 0; c < BNT; ++c)
-                  if (m0 + c < p.M) ((int32_t *)p.y)[(size_t)(m0 + c) * p.N + n] = sums[c];
-              } else {
-                const float sw = __ldg(p.w_scale + n);
-                const float sx0 = __ldg(p.x_scale);
-                const float b = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
+                  if (m0 + c < p.M) ((int32_t *)p.y)[(size_t)(m0 + c) * p.N + wrow] = sums[c];
+              }
+            } else {
+              const float sw = valid ? __ldg(p.w_scale + wrow) : 0.0f;
+              const float sx0 = __ldg(p.x_scale);
+              const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + wrow)) : 0.0f;
 #pragma unroll
-                for (int c = 0; c < BNT; ++c)
-                  if (m0 + c < p.M) {
-                    const float sc = (p.xs_per_token ? __ldg(p.x_scale + m0 + c) : sx0) * sw;
-                    ((uint16_t *)p.y)[(size_t)(m0 + c) * p.N + n] = f32_to_bf16_bits(fmaf((float)sums[c], sc, b));
+              for (int c = 0; c < BNT; c += 16) {  // fully unrolled: sums[] stays in registers
+                if (ok) {
+                  float v[16];
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) {
+                    const int m = m0 + c + e;
+                    const float sx = p.xs_per_token ? (m < p.M ? __ldg(p.x_scale + m) : 0.0f) : sx0;
+                    v[e] = fmaf((float)sums[c + e], sx * sw, b);
                   }
+                  ok = emit16(m0, c, ochan, v);
+                }
               }
             }
           } else {
@@ -674,7 +809,33 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   if (S > 1) {  // one unit per CTA: sum the partial tiles of the cluster
     cluster_sync();
-    if (warp >= 4) {
+    if (warp >= 4 && p.glu) {
+      // merged gate_up: a unit is 4 gate rows of one token plus the same 4 up rows (64 rows on)
+      const int ct = threadIdx.x - 128;  // 512 threads
+      const uint32_t base = smem_u32(smem);
+      const int u = blockIdx.x, tt = u % p.ntiles, m0 = (u / p.ntiles) * BNT;
+      constexpr int UG = BNT * 64 / 4;
+      const int u0 = (int)((int64_t)split * UG / S), u1 = (int)((int64_t)(split + 1) * UG / S);
+      for (int g4 = u0 + ct; g4 < u1; g4 += 512) {
+        const int jj = g4 / 16, nq = (g4 % 16) * 4;
+        const uint32_t wg = (uint32_t)(jj * C::BM + nq), wu = wg + 64;  // word offsets in the tile
+        uint32_t ag[4] = {0, 0, 0, 0}, au[4] = {0, 0, 0, 0};
+        for (int r = 0; r < S; ++r) {  // fixed order: deterministic
+          const uint4 vg = ld_dsmem_v4(map_peer_smem(base + 4u * wg, (uint32_t)r));
+          const uint4 vu = ld_dsmem_v4(map_peer_smem(base + 4u * wu, (uint32_t)r));
+          const uint32_t g4v[4] = {vg.x, vg.y, vg.z, vg.w}, u4v[4] = {vu.x, vu.y, vu.z, vu.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ag[e] = kI8 ? (uint32_t)((int32_t)ag[e] + (int32_t)g4v[e])
+                        : __float_as_uint(__uint_as_float(ag[e]) + __uint_as_float(g4v[e]));
+            au[e] = kI8 ? (uint32_t)((int32_t)au[e] + (int32_t)u4v[e])
+                        : __float_as_uint(__uint_as_float(au[e]) + __uint_as_float(u4v[e]));
+          }
+        }
+        const int m = m0 + jj;
+        if (m < p.M) glu_store4<MODE>(p, m, tt * 64 + nq, ag, au);
+      }
+    } else if (warp >= 4) {
       const int ct = threadIdx.x - 128;  // 512 threads
       const uint32_t base = smem_u32(smem);
       const int u = blockIdx.x, n0 = (u % p.ntiles) * C::BM, m0 = (u / p.ntiles) * BNT;
@@ -710,31 +871,55 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   if (g.M == 0) return cudaSuccess;
   using C = Fp8Cfg;
   CUtensorMap ta, tb;
+  // glu: the weight has 2N rows and a tile takes 128 gate rows plus their 128 up rows (two boxes)
+  const int64_t wrows = g.glu ? 2 * g.N : g.N;
   if (!make_map(&ta, g.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.M, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.N, g.K, C::BK, C::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wrows, g.K, C::BK, g.glu ? C::BN / 2 : C::BN,
+                CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static cudaError_t attr = set_smem(k_fp8_gemm, C::SMEM);
   if (attr != cudaSuccess) return attr;
-  const int mtiles = (int)((g.M + C::BM - 1) / C::BM), ntiles = (int)((g.N + C::BN - 1) / C::BN);
+  // glu: an output tile is 128 channels (n0 counts the 256 gate+up columns of the MMA tile)
+  const int mtiles = (int)((g.M + C::BM - 1) / C::BM);
+  const int ntiles = g.glu ? (int)(g.N / (C::BN / 2)) : (int)((g.N + C::BN - 1) / C::BN);
   const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.w_scale, g.x_scale, g.bias,
-              (uint16_t *)g.y, dev.status};
+  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.glu, g.w_scale, g.x_scale,
+              g.bias, (uint16_t *)g.y, dev.status};
   return launch_kernel(k_fp8_gemm, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, p);
 }
 
-int w8_swap_bnt(int64_t M) {
-  return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+// Token tile (MMA N) of the W8A16 swap-AB kernel.  Up to 128 tokens the tile
+// covers the batch.  Above that both 128 and 256 are candidates: a 256-token
+// tile converts each weight tile once for twice the tokens, a 128-token tile
+// makes twice the output tiles (fewer or no K splits, finer waves).  The cost
+// of each is estimated as waves x k-blocks per CTA x per-block cost, where a
+// 256-token block costs 1.63 times a 128-token block (the ratio of their
+// per-unit times measured on the 7B gate_up shape, K = 3584, N = 37888).
+int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms) {
+  if (M <= 128) return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  const int64_t kb = (K + 63) / 64, nt = (N + 127) / 128;
+  auto cost = [&](int bnt, double per_block) {
+    const int64_t units = nt * ((M + bnt - 1) / bnt);
+    const int64_t s = w8_swap_splits(units, K, sms, bnt);
+    const int64_t waves = (units * s + sms - 1) / sms;
+    return (double)waves * (double)((kb + s - 1) / s) * per_block;
+  };
+  return cost(128, 1.0) < cost(256, 1.63) ? 128 : 256;
 }
 int i8_swap_bnt(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
 // Split-K factor: CTAs of a cluster that share one output tile when the tiles
-// alone cannot fill the GPU.
-int w8_swap_splits(int64_t tiles, int64_t K, int sms) {
+// alone cannot fill the GPU.  Each CTA of a cluster stages a 128 x BNT fp32
+// partial tile and reduces 1/S of the tile over all S peers, so for token tiles
+// of 128 or more the split is capped at 4 and keeps at least 8 k-blocks a CTA
+// (measured: q/down projections at 256 tokens took twice as long with 8 splits).
+int w8_swap_splits(int64_t tiles, int64_t K, int sms, int bnt) {
   const int64_t kb = (K + 63) / 64;
   if (tiles * 4 >= (int64_t)sms * 3) return 1;
   int64_t s = sms / tiles;
-  if (s > 8) s = 8;
-  if (s > kb / 2) s = kb / 2;
+  const int64_t cap = bnt >= 128 ? 4 : 8, min_blocks = bnt >= 128 ? 8 : 2;
+  if (s > cap) s = cap;
+  if (s > kb / min_blocks) s = kb / min_blocks;
   return s < 1 ? 1 : (int)s;
 }
 
@@ -742,24 +927,27 @@ template <int BNT, int QT, int MODE>
 static cudaError_t launch_dq_t(const GemmArgs &g, const void *xb, const DeviceInfo &dev, cudaStream_t st) {
   using C = DqCfg<BNT>;
   CUtensorMap tw, tx;
-  if (!make_map(&tw, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.N, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  // glu: the weight has 2N rows; a tile loads 64 gate rows and their 64 up rows (two boxes)
+  const int64_t wrows = g.glu ? 2 * g.N : g.N;
+  if (!make_map(&tw, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wrows, g.K, C::BK, g.glu ? 64 : C::BM,
+                CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&tx, xb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, BNT, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static cudaError_t attr = set_smem(k_w8_dq<BNT, QT, MODE>, C::SMEM);
   if (attr != cudaSuccess) return attr;
-  const int ntiles = (int)((g.N + C::BM - 1) / C::BM);
+  const int ntiles = g.glu ? (int)(g.N / 64) : (int)((g.N + C::BM - 1) / C::BM);
   const int units = ntiles * (int)((g.M + BNT - 1) / BNT);
-  const int S = w8_swap_splits(units, g.K, dev.sms);
+  const int S = w8_swap_splits(units, g.K, dev.sms, BNT);
   const int G = S > 1 ? units : (units < dev.sms ? units : dev.sms);
-  SwapParams p{(int)g.M, (int)g.N,  (int)g.K, g.x_scale_per_token, S, units, ntiles, g.w_scale, g.x_scale,
-               g.bias,     g.y,        dev.status};
+  SwapParams p{(int)g.M, (int)g.N, (int)g.K, g.x_scale_per_token, g.glu, S,  units,
+               ntiles,    g.w_scale, g.x_scale, g.bias,  g.y,        dev.status};
   return launch_kernel(k_w8_dq<BNT, QT, MODE>, dim3((unsigned)G, 1, (unsigned)S), dim3(C::THREADS), C::SMEM, st,
                        (unsigned)S, tw, tx, p);
 }
 
 template <int QT>
 static cudaError_t launch_w8a16_q(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
-  switch (w8_swap_bnt(g.M)) {
+  switch (w8_swap_bnt(g.M, g.glu ? 2 * g.N : g.N, g.K, dev.sms)) {
     case 16: return launch_dq_t<16, QT, kSwapW8A16>(g, g.a, dev, st);
     case 32: return launch_dq_t<32, QT, kSwapW8A16>(g, g.a, dev, st);
     case 64: return launch_dq_t<64, QT, kSwapW8A16>(g, g.a, dev, st);

@@ -72,6 +72,7 @@ struct GemmArgs {
   const uint16_t *bias;   // [N] or null
   void *y;                // [M,N] BF16, or int32 for kI8Raw
   int x_scale_per_token = 0;  // x_scale holds one scale per token row (dynamic W8A8)
+  int glu = 0;  // merged gate_up: qw/w_scale/bias have 2N rows (gate rows first), y = silu(gate) * up [M, N]
 };
 
 // Mixed KV cache (kv_kernels.cu): INT8 keys with float16 group-32 scales,
@@ -94,9 +95,9 @@ cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStrea
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st);
-int w8_swap_bnt(int64_t M);
+int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms);
 int i8_swap_bnt(int64_t M);
-int w8_swap_splits(int64_t tiles, int64_t K, int sms);
+int w8_swap_splits(int64_t tiles, int64_t K, int sms, int bnt);
 
 // INT8 operand preparation for the tensor-core INT8 path (quant_kernels.cu)
 cudaError_t launch_quantize_act_i8bf16(int64_t M, int64_t K, const void *x, const float *s, void *out, int sms,

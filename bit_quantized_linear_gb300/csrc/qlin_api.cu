@@ -19,6 +19,17 @@ static constexpr int kMaxDevices = 64;
 static DeviceInfo g_dev[kMaxDevices];
 static std::mutex g_dev_mu;
 
+// SM count of the current device for host-side tile choices that name a
+// kernel without launching it: the cached value, else 152 (GB300).
+static int sm_count() {
+  int d = -1;
+  if (cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev[d].device == d && g_dev[d].sms > 0) return g_dev[d].sms;
+  }
+  return 152;
+}
+
 // Caches the SM count, compute capability and status-word address of the
 // current device.  Returns QLIN_OK or an error status.
 static qlin_status current_device(DeviceInfo **out) {
@@ -55,6 +66,13 @@ static qlin_status check_linear_shape(int64_t M, int64_t K, int64_t N) {
   return QLIN_OK;
 }
 
+// Merged gate_up: I output channels (a multiple of 128: both kernels pair whole
+// gate and up row blocks), weight rows 2I.
+static qlin_status check_glu_shape(int64_t M, int64_t K, int64_t I) {
+  if (I < 128 || (I % 128) || I > (int64_t)1 << 30) return QLIN_ERR_INVALID_ARG;
+  return check_linear_shape(M, K, 2 * I);
+}
+
 }  // namespace qlin
 
 using namespace qlin;
@@ -71,11 +89,17 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_QUANTIZE_WEIGHT: return "k_quantize_weight";
     case QLIN_OP_ACT_SCALE: return "k_absmax_bf16+k_scale_finalize";
     case QLIN_OP_QUANTIZE_ACT: return "k_quantize_act";
+    case QLIN_OP_W8A16_GATE_UP_SILU:
+      if (check_glu_shape(M, K, N)) return "invalid";
+      return qlin_kernel_name(QLIN_OP_W8A16_LINEAR, qtype, M, K, 2 * N);
+    case QLIN_OP_W8A8_GATE_UP_SILU:
+      if (check_glu_shape(M, K, N)) return "invalid";
+      return qlin_kernel_name(QLIN_OP_W8A8_LINEAR, qtype, M, K, 2 * N);
     case QLIN_OP_W8A16_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
       static const char *names[5] = {"k_w8_dq<16>", "k_w8_dq<32>", "k_w8_dq<64>", "k_w8_dq<128>", "k_w8_dq<256>"};
-      const int b = w8_swap_bnt(M);
+      const int b = w8_swap_bnt(M, N, K, sm_count());
       return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : b == 128 ? 3 : 4];
     }
     case QLIN_OP_I8_GEMM_S32: {
@@ -148,7 +172,10 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
       return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256) + round_up((size_t)M * 4, 256);
     case QLIN_OP_KV_STORE_MIXED:
     case QLIN_OP_KV_LOAD_MIXED:
+    case QLIN_OP_W8A16_GATE_UP_SILU:
       return 0;
+    case QLIN_OP_W8A8_GATE_UP_SILU:
+      return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256);
   }
   return (size_t)-1;
 }
@@ -278,6 +305,48 @@ qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, co
   if (launch_i8_to_bf16(M, K, qx, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
   GemmArgs g{kI8Raw, QLIN_INT8, M, K, N, ws, qw, nullptr, nullptr, nullptr, acc};
   return from_cuda(launch_i8_swap(g, ws, true, *dev, st));
+}
+
+qlin_status qlin_w8a16_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int64_t I, const void *x,
+                                    const void *qw, const float *w_scale, const void *bias, void *y, void *ws,
+                                    size_t ws_bytes, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = check_glu_shape(M, K, I)) return s;
+  if (!qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias))) return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
+  (void)ws;
+  (void)ws_bytes;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  GemmArgs g{kW8A16, qtype, M, K, I, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
+  g.glu = 1;
+  return from_cuda(launch_w8a16_swap(g, *dev, (cudaStream_t)stream));
+}
+
+qlin_status qlin_w8a8_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int64_t I, const void *x,
+                                   const float *input_scale, const void *qw, const float *w_scale,
+                                   const void *bias, void *y, void *ws, size_t ws_bytes, qlin_stream_t stream) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = check_glu_shape(M, K, I)) return s;
+  if (!input_scale || !qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias)) ||
+      ((uintptr_t)input_scale & 3u))
+    return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
+  const size_t need = qlin_workspace_bytes(QLIN_OP_W8A8_GATE_UP_SILU, qtype, M, K, I);
+  if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
+  DeviceInfo *dev;
+  if (qlin_status s = current_device(&dev)) return s;
+  if (M == 0) return QLIN_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  GemmArgs g{kW8A8, qtype, M, K, I, ws, qw, w_scale, input_scale, (const uint16_t *)bias, y};
+  g.glu = 1;
+  if (qtype == QLIN_E4M3) {
+    if (launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
+    return from_cuda(launch_fp8_gemm(g, *dev, st));
+  }
+  if (launch_quantize_act_i8bf16(M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
+  return from_cuda(launch_i8_swap(g, ws, false, *dev, st));
 }
 
 // Shared argument checks of the two KV-cache entry points.

@@ -91,6 +91,7 @@ class Linear:
     outliers: bool = False
     workload: str = ""
     layer: int = 0
+    glu: bool = False  # merged gate_up [N = 2I, K] with the SiLU * up epilogue: output [M, N/2]
 
 
 @dataclass
@@ -143,14 +144,25 @@ STACK_SHAPES = [("q_proj", 2048, 2048), ("k_proj", 2048, 256), ("v_proj", 2048, 
                 ("o_proj", 2048, 2048), ("gate_up_proj", 2048, 22016), ("down_proj", 11008, 2048)]
 
 
-def stack_linears(phase: str) -> list[Linear]:
-    """36 layers x 6 linears; decode = INT8 W8A16 at M=256, prefill = E4M3 W8A8 at M=8192."""
+# The same layer with the merged projections of the model's four quantized linears
+# per layer (tiny-vLLM README, quality check: 112 target layers for 28 layers):
+# merged qkv, o, merged gate_up with the SiLU * up epilogue, down.
+STACK_FUSED_SHAPES = [("qkv_proj", 2048, 2560, False), ("o_proj", 2048, 2048, False),
+                      ("gate_up_silu", 2048, 22016, True), ("down_proj", 11008, 2048, False)]
+
+
+def stack_linears(phase: str, fused: bool = False) -> list[Linear]:
+    """36 layers x 6 linears (or x 4 merged ones when fused); decode = INT8 W8A16 at
+    M=256, prefill = E4M3 W8A8 at M=8192."""
     if phase == "decode":
         M, qt, form = 256, "int8", "w8a16"
     elif phase == "prefill":
         M, qt, form = 8192, "e4m3", "w8a8"
     else:
         raise KeyError(phase)
+    if fused:
+        return [Linear(s, K, N, M, qt, form, workload=f"{STACK}-fused-{phase}", layer=l, glu=g)
+                for l in range(STACK_LAYERS) for (s, K, N, g) in STACK_FUSED_SHAPES]
     return [Linear(s, K, N, M, qt, form, workload=f"{STACK}-{phase}", layer=l)
             for l in range(STACK_LAYERS) for (s, K, N) in STACK_SHAPES]
 

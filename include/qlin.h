@@ -74,7 +74,9 @@ typedef enum {
   QLIN_OP_I8_GEMM_S32 = 5,
   QLIN_OP_W8A8_DYNAMIC_LINEAR = 6,
   QLIN_OP_KV_STORE_MIXED = 7, /* for qlin_kernel_name: M = tokens, K = head_dim, N = kv heads */
-  QLIN_OP_KV_LOAD_MIXED = 8
+  QLIN_OP_KV_LOAD_MIXED = 8,
+  QLIN_OP_W8A16_GATE_UP_SILU = 9, /* N = the intermediate size I (output channels) */
+  QLIN_OP_W8A8_GATE_UP_SILU = 10
 } qlin_op;
 
 /*
@@ -223,6 +225,34 @@ qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, co
 qlin_status qlin_w8a8_linear_noalloc(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
                                      const float *input_scale, const void *qw, const float *w_scale,
                                      const void *bias, void *y, qlin_stream_t stream);
+
+/*
+ * Merged gate_up linear with the SiLU * up epilogue.  The "tiny-vLLM" README's
+ * quality check counts four quantized linears per layer of its 28-layer model
+ * (112 target layers): merged qkv, o, merged gate_up and down.  The model
+ * family's MLP is down(silu(gate(x)) * up(x)); these entry points compute the
+ * merged gate_up linear and its activation in one kernel, so the [M, 2I]
+ * intermediate never reaches memory:
+ *   qw [2I, K] codes with the gate rows [0, I) above the up rows [I, 2I)
+ *   (the export layout of a merged gate_up projection), w_scale [2I] fp32,
+ *   bias [2I] BF16 or NULL;
+ *   g = the linear's fp32 output for row n, u = for row I + n (bias added),
+ *   y[m, n] = bf16( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),  y [M, I].
+ * g and u are not rounded to BF16 in between.  I must be a multiple of 128.
+ * qlin_w8a16_gate_up_silu takes BF16 x like qlin_w8a16_linear (no workspace);
+ * qlin_w8a8_gate_up_silu quantizes x with the static input_scale like
+ * qlin_w8a8_linear (workspace: qlin_workspace_bytes(QLIN_OP_W8A8_GATE_UP_SILU,
+ * qtype, M, K, I) bytes).  Other requirements as for those linears.
+ * The merged qkv linear needs no entry point of its own: its per-channel
+ * scales make it qlin_w8a16_linear / qlin_w8a8_linear over the concatenated
+ * weight [Nq + Nk + Nv, K].
+ */
+qlin_status qlin_w8a16_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int64_t I, const void *x,
+                                    const void *qw, const float *w_scale, const void *bias, void *y, void *ws,
+                                    size_t ws_bytes, qlin_stream_t stream);
+qlin_status qlin_w8a8_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int64_t I, const void *x,
+                                   const float *input_scale, const void *qw, const float *w_scale,
+                                   const void *bias, void *y, void *ws, size_t ws_bytes, qlin_stream_t stream);
 
 /*
  * Mixed KV-cache quantization ("Nano-vLLM-MoE" README, section "KV cache

@@ -95,6 +95,15 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert capi.qlin_kernel_name(capi.QLIN_OP_KV_STORE_MIXED, 0, 8, 128, 4) == "k_kv_store_mixed<128>"
     assert capi.qlin_kernel_name(capi.QLIN_OP_KV_LOAD_MIXED, 0, 8, 64, 4) == "k_kv_load_mixed<64>"
     assert capi.qlin_kernel_name(capi.QLIN_OP_KV_LOAD_MIXED, 0, 8, 80, 4) == "invalid"
+    # merged gate_up: I a multiple of 128; W8A8 needs its workspace
+    assert L.qlin_w8a16_gate_up_silu(0, 4, 64, 192, good, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_gate_up_silu(0, 4, 64, 0, good, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a16_gate_up_silu(0, 4, 64, 128, odd, good, good, None, good, None, 0, None) == INV
+    assert L.qlin_w8a8_gate_up_silu(1, 4, 64, 128, good, good, good, good, None, good, None, 0, None) == WS
+    assert L.qlin_w8a8_gate_up_silu(1, 4, 64, 100, good, good, good, good, None, good, good, 4096, None) == INV
+    assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A8_GATE_UP_SILU, "e4m3", 4, 64, 128) >= 256
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_GATE_UP_SILU, 0, 1, 3584, 18944) == "k_w8_dq<16>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 11008) == "k_quantize_act+k_fp8_gemm"
 
 
 def test_no_device_is_reported_not_crashed(capi):
