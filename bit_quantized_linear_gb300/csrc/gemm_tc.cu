@@ -102,9 +102,16 @@ struct Fp8Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
+// MC = 2: the CTAs of a 2-CTA cluster take the two m-tiles of a pair with the
+// same n-tile; each loads its own A tile and half of the shared B tile, which
+// TMA multicasts into both CTAs, so every B byte leaves L2 once per pair.  A
+// stage may be refilled only when both CTAs' MMAs have read it: the MMA
+// commits arrive on the stage's empty barrier in both CTAs.
+template <int MC>
 __global__ void __launch_bounds__(384, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Fp8Params p) {
   using C = Fp8Cfg;
+  static_assert(MC == 1 || MC == 2, "cluster of one or two CTAs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint64_t *full = (uint64_t *)(smem + C::BAR_OFF);
@@ -114,13 +121,18 @@ __global__ void __launch_bounds__(384, 1)
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (p.K + C::BK - 1) / C::BK;
-  const int tiles = p.mtiles * p.ntiles, G = gridDim.x;
-  const int my_tiles = ((int)blockIdx.x < tiles) ? (tiles - (int)blockIdx.x + G - 1) / G : 0;
+  // work items: tiles (MC = 1) or tile pairs (MC = 2: m-tiles 2q, 2q+1 of one n-tile)
+  const int rank = MC == 2 ? (int)cluster_ctarank() : 0;
+  const int mgroups = (p.mtiles + MC - 1) / MC;
+  const int items = mgroups * p.ntiles, G = gridDim.x / MC, cid = blockIdx.x / MC;
+  const int my_tiles = (cid < items) ? (items - cid + G - 1) / G : 0;
+  auto tile_m0 = [&](int t) { return ((t / p.ntiles) * MC + rank) * C::BM; };
+  auto tile_n0 = [&](int t) { return (t % p.ntiles) * C::BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC);  // the MMA commits of every CTA that reads the stage's B tile
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -135,6 +147,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (MC == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
   pdl_trigger();
@@ -143,8 +156,8 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       int i = 0;
       for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
-        const int t = blockIdx.x + j * G;
-        const int m0 = (t / p.ntiles) * C::BM, n0 = (t % p.ntiles) * C::BN;
+        const int t = cid + j * G;
+        const int m0 = tile_m0(t), n0 = tile_n0(t);
         for (int kb = 0; kb < nkb; ++kb, ++i) {
           const int s = i % C::STAGES;
           if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
@@ -154,11 +167,14 @@ __global__ void __launch_bounds__(384, 1)
           uint8_t *st = smem + s * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           tma_load_2d(&tm_a, &full[s], st, kb * C::BK, m0);
-          if (p.glu) {  // gate rows n0/2.. and the matching up rows N + n0/2.. (box of 128 rows each)
-            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, n0 / 2);
-            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, p.N + n0 / 2);
+          // B: two boxes of 128 rows; glu: the gate rows n0/2.. and the matching up rows N + n0/2..
+          const int b0 = p.glu ? n0 / 2 : n0, b1 = p.glu ? p.N + n0 / 2 : n0 + C::BN / 2;
+          if constexpr (MC == 2) {  // this CTA loads box `rank` for both CTAs of the pair
+            tma_load_2d_mc(&tm_b, &full[s], st + C::A_BYTES + rank * (C::B_BYTES / 2), kb * C::BK,
+                           rank ? b1 : b0, (uint16_t)0x3);
           } else {
-            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, n0);
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, b0);
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, b1);
           }
         }
       }
@@ -188,7 +204,8 @@ __global__ void __launch_bounds__(384, 1)
           mma_fp8(dt, ad + 2, bd + 2, C::IDESC, 1u);
           mma_fp8(dt, ad + 4, bd + 4, C::IDESC, 1u);
           mma_fp8(dt, ad + 6, bd + 6, C::IDESC, 1u);
-          mma_commit(&empty[s]);
+          if constexpr (MC == 2) mma_commit_mc(&empty[s], (uint16_t)0x3);
+          else mma_commit(&empty[s]);
         }
         if (!ok) break;
         mma_commit(&acc_full[b]);
@@ -204,8 +221,8 @@ __global__ void __launch_bounds__(384, 1)
     const float sx = p.xs_per_token ? 1.0f : __ldg(p.x_scale);
     bool ok = true;
     for (int j = 0; j < my_tiles && ok; ++j) {
-      const int t = blockIdx.x + j * G, b = j & 1;
-      const int m0 = (t / p.ntiles) * C::BM, n0 = (t % p.ntiles) * C::BN;
+      const int t = cid + j * G, b = j & 1;
+      const int m0 = tile_m0(t), n0 = tile_n0(t);
       ok = mbar_wait(&acc_full[b], (j >> 1) & 1, abort_flag);
       tc_fence_after();
       // tcgen05.ld is warp-collective: every lane of the warp takes the same path
@@ -290,6 +307,9 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // neither CTA of a pair leaves while the other may still multicast into it or
+  // arrive on its barriers (every wait above is bounded, so both get here)
+  if constexpr (MC == 2) cluster_sync();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -873,19 +893,27 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   CUtensorMap ta, tb;
   // glu: the weight has 2N rows and a tile takes 128 gate rows plus their 128 up rows (two boxes)
   const int64_t wrows = g.glu ? 2 * g.N : g.N;
+  // B is loaded as two boxes of 128 rows (two halves of the 256-row tile)
   if (!make_map(&ta, g.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.M, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wrows, g.K, C::BK, g.glu ? C::BN / 2 : C::BN,
+      !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wrows, g.K, C::BK, C::BN / 2,
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static cudaError_t attr = set_smem(k_fp8_gemm, C::SMEM);
-  if (attr != cudaSuccess) return attr;
   // glu: an output tile is 128 channels (n0 counts the 256 gate+up columns of the MMA tile)
   const int mtiles = (int)((g.M + C::BM - 1) / C::BM);
   const int ntiles = g.glu ? (int)(g.N / (C::BN / 2)) : (int)((g.N + C::BN - 1) / C::BN);
-  const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
   Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.glu, g.w_scale, g.x_scale,
               g.bias, (uint16_t *)g.y, dev.status};
-  return launch_kernel(k_fp8_gemm, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, p);
+  if (mtiles >= 2) {  // pairs of m-tiles share their B tiles (2-CTA clusters, TMA multicast)
+    static cudaError_t attr2 = set_smem(k_fp8_gemm<2>, C::SMEM);
+    if (attr2 != cudaSuccess) return attr2;
+    const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
+    const int grid = 2 * (items < pairs ? items : pairs);
+    return launch_kernel_x(k_fp8_gemm<2>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 2, ta, tb, p);
+  }
+  static cudaError_t attr = set_smem(k_fp8_gemm<1>, C::SMEM);
+  if (attr != cudaSuccess) return attr;
+  const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
+  return launch_kernel(k_fp8_gemm<1>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, p);
 }
 
 // Token tile (MMA N) of the W8A16 swap-AB kernel.  Up to 128 tokens the tile

@@ -47,6 +47,29 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// As launch_kernel, with a cluster shape along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_x(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            unsigned cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = cluster_x;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_quantize_weight(int qtype, int64_t N, int64_t K, const float *w, void *qw,
                                    float *s, cudaStream_t st);
 cudaError_t launch_act_scale(int qtype, int64_t rows, int64_t K, const void *x, float *scale,

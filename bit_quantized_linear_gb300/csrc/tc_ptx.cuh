@@ -173,6 +173,27 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 // Arrives on `bar` once every tcgen05.mma issued so far by this thread completes.
+// TMA 2D load multicast to the CTAs of the cluster in `cta_mask`: the tile lands
+// at the same shared-memory offset in each, and each one's mbarrier at `bar`'s
+// offset receives the complete_tx bytes.
+__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap *tm, uint64_t *bar, void *dst, int c0, int c1,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
+      : "memory");
+}
+
+// tcgen05.commit arriving on the mbarrier at `bar`'s offset in every CTA of `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
