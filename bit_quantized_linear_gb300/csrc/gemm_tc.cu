@@ -323,13 +323,17 @@ __global__ void __launch_bounds__(384, 1)
 //
 // Modes:  W8A16: B = BF16 activations, fp32 accumulation over all of K,
 //                epilogue y = acc * s_w[n] + bias[n].
+//         I8 fused: B = raw BF16 activations; the converter quad that takes a
+//                k-block also quantizes that block's activation tile in place
+//                (static per-tensor scale) into integer-valued BF16 before it
+//                releases the block to the MMA, so the linear is one kernel.
 //         I8:    B = activation codes stored as integer-valued BF16; the MMA
 //                accumulates fp32 over chunks of 512 k, where every partial sum
 //                is an integer below 127*127*512 < 2^23 and therefore exact; the
 //                epilogue warps add each chunk into int32 registers, so the full
 //                accumulator is the exact integer sum.  Output: raw int32, or
 //                y = acc * (s_x * s_w[n]) + bias[n].
-enum SwapMode { kSwapW8A16 = 0, kSwapI8Scaled = 1, kSwapI8Raw = 2 };
+enum SwapMode { kSwapW8A16 = 0, kSwapI8Scaled = 1, kSwapI8Raw = 2, kSwapI8Fused = 3 };
 
 struct SwapParams {
   int M, N, K;       // N: output channels (the intermediate size I when glu)
@@ -345,7 +349,7 @@ struct SwapParams {
   unsigned *status;
 };
 
-template <int BNT>
+template <int BNT, int MODE = 0>
 struct DqCfg {
   static constexpr int BM = 128, BK = 64;
   static constexpr int RAW_BYTES = BM * BK;     // 8-bit weight tile, 64-byte swizzle
@@ -372,7 +376,8 @@ struct DqCfg {
   //                  wait a_full)
   //   activations   (ISSUERS MMA threads)             X  % ISSUERS == 0
   static constexpr int NA = ACOL == 128 ? 12 : 6;  // A stages, 32 columns (64 BF16 k) each
-  static constexpr int X = BNT <= 32 ? 16 : BNT == 64 ? 8 : BNT == 128 ? 8 : 4;
+  //   activations   (fused I8: the 3 quads wait x_full too) X % (QUADS * ISSUERS) == 0
+  static constexpr int X = MODE == 3 ? (BNT <= 32 ? 18 : 12) : BNT <= 32 ? 16 : BNT == 64 ? 8 : BNT == 128 ? 8 : 4;
   static constexpr int RING = 200 * 1024;
   static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
   static constexpr int R = (R0 > 15 ? 15 : R0) / 3 * 3;  // raw stages
@@ -385,6 +390,7 @@ struct DqCfg {
   static_assert(R % QUADS == 0 && R >= 6, "raw ring depth: multiple of the converter quads");
   static_assert(NA % (QUADS * ISSUERS) == 0, "A ring depth: multiple of quads x issuers");
   static_assert(X % ISSUERS == 0, "activation ring depth: multiple of the MMA issuers");
+  static_assert(MODE != 3 || X % (QUADS * ISSUERS) == 0, "fused activation ring: multiple of quads x issuers");
   static_assert(ND * DSTRIDE <= ACOL && ACOL + NA * 32 <= 512, "TMEM columns");
   static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -430,7 +436,8 @@ __device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const 
   if constexpr (MODE == kSwapI8Raw) {
     *reinterpret_cast<uint4 *>((int32_t *)p.y + (size_t)m * p.N + n) = make_uint4(v[0], v[1], v[2], v[3]);
   } else {
-    const float sx = MODE == kSwapI8Scaled ? __ldg(p.x_scale + (p.xs_per_token ? m : 0)) : 1.0f;
+    const float sx = MODE == kSwapI8Scaled || MODE == kSwapI8Fused ? __ldg(p.x_scale + (p.xs_per_token ? m : 0))
+                                                                     : 1.0f;
     uint32_t o[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -453,7 +460,8 @@ __device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const 
 template <int MODE>
 __device__ __forceinline__ void glu_store4(const SwapParams &p, int m, int ch, const uint32_t (&g)[4],
                                            const uint32_t (&u)[4]) {
-  const float sx = MODE == kSwapI8Scaled ? __ldg(p.x_scale + (p.xs_per_token ? m : 0)) : 1.0f;
+  const float sx = MODE == kSwapI8Scaled || MODE == kSwapI8Fused ? __ldg(p.x_scale + (p.xs_per_token ? m : 0))
+                                                                   : 1.0f;
   float y[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -472,8 +480,9 @@ __device__ __forceinline__ void glu_store4(const SwapParams &p, int m, int ch, c
 template <int BNT, int QT, int MODE>
 __global__ void __launch_bounds__(640, 1)
     k_w8_dq(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, SwapParams p) {
-  using C = DqCfg<BNT>;
+  using C = DqCfg<BNT, MODE>;
   constexpr bool kI8 = MODE != kSwapW8A16;
+  constexpr bool kXQ = MODE == kSwapI8Fused;  // quantize the activation tiles in place
   constexpr int CH = kI8 ? 8 : (1 << 30);  // k-blocks per exactly accumulated chunk
   static_assert(!kI8 || BNT <= 64, "int32 sums live in registers");
   extern __shared__ uint8_t smem_raw[];
@@ -629,6 +638,8 @@ __global__ void __launch_bounds__(640, 1)
     const int quad = (warp - 4) >> 2, q4 = warp & 3, row = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     bool ok = true;
+    Scale xsc{1.0f, 1.0f, true};
+    if constexpr (kXQ) xsc = make_scale(__ldg(p.x_scale));
     for (int i = quad; i < total; i += C::QUADS) {
       const int r = i % C::R, sa = i % C::NA;
       if (!mbar_wait(&raw_full[r], (i / C::R) & 1, abort_flag)) {
@@ -646,6 +657,31 @@ __global__ void __launch_bounds__(640, 1)
       for (int c = 0; c < 4; ++c) convert16<QT>(raw[c], words + 8 * c);
       __syncwarp();
       if (lane == 0) mbar_arrive(&raw_empty[r]);
+      if constexpr (kXQ) {
+        // quantize this block's activation tile in place: thread `row` takes BNT
+        // consecutive bytes (BNT / 2 BF16 values) of the BNT x 128-byte tile; the
+        // 128-byte swizzle only permutes elements, so the in-place map is the same
+        const int sxs = i % C::X;
+        if (!mbar_wait(&x_full[sxs], (i / C::X) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t xb = smem_u32(xs + sxs * C::X_BYTES) + row * BNT;
+#pragma unroll
+        for (int c = 0; c < BNT / 16; ++c) {
+          const uint4 v = lds128(xb + 16 * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(w[e] & 0xFFFFu), xsc);
+            const float hi = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(w[e] >> 16), xsc);
+            o[e] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+          }
+          sts128(xb + 16 * c, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+      }
       if (i >= C::NA && !mbar_wait(&a_empty[sa], ((i / C::NA) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
@@ -953,7 +989,7 @@ int w8_swap_splits(int64_t tiles, int64_t K, int sms, int bnt) {
 
 template <int BNT, int QT, int MODE>
 static cudaError_t launch_dq_t(const GemmArgs &g, const void *xb, const DeviceInfo &dev, cudaStream_t st) {
-  using C = DqCfg<BNT>;
+  using C = DqCfg<BNT, MODE>;
   CUtensorMap tw, tx;
   // glu: the weight has 2N rows; a tile loads 64 gate rows and their 64 up rows (two boxes)
   const int64_t wrows = g.glu ? 2 * g.N : g.N;
@@ -991,8 +1027,19 @@ cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStre
 
 // INT8 x INT8 on the BF16 tensor cores; `xb` holds the activation codes as
 // integer-valued BF16 [M, K].  raw: int32 accumulator out; else scaled BF16.
-cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st) {
+// fused: `xb` is the BF16 activation itself, quantized inside the kernel with
+// the static scale (one token tile, M <= 64).
+cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st,
+                           bool fused) {
   if (g.M == 0) return cudaSuccess;
+  if (fused) {
+    if (raw || g.x_scale_per_token || g.M > 64) return cudaErrorInvalidValue;
+    switch (i8_swap_bnt(g.M)) {
+      case 16: return launch_dq_t<16, QLIN_INT8, kSwapI8Fused>(g, xb, dev, st);
+      case 32: return launch_dq_t<32, QLIN_INT8, kSwapI8Fused>(g, xb, dev, st);
+      default: return launch_dq_t<64, QLIN_INT8, kSwapI8Fused>(g, xb, dev, st);
+    }
+  }
   switch (i8_swap_bnt(g.M)) {
     case 16:
       return raw ? launch_dq_t<16, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)

@@ -117,7 +117,8 @@ cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStrea
 // tcgen05 kernels (gemm_tc.cu)
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
-cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st);
+cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const DeviceInfo &dev, cudaStream_t st,
+                           bool fused = false);
 int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms);
 int i8_swap_bnt(int64_t M);
 int w8_swap_splits(int64_t tiles, int64_t K, int sms, int bnt);

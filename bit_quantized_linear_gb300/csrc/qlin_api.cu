@@ -66,6 +66,12 @@ static qlin_status check_linear_shape(int64_t M, int64_t K, int64_t N) {
   return QLIN_OK;
 }
 
+// INT8 W8A8 with a static scale and one token tile (M <= 64): the GEMM kernel
+// quantizes its activation tiles itself (one kernel, no workspace round trip).
+// Larger batches quantize once in a separate pass, which every output tile then
+// reuses.
+static bool i8_fused_quant(int64_t M) { return M <= 64; }
+
 // Merged gate_up: I output channels (a multiple of 128: both kernels pair whole
 // gate and up row blocks), weight rows 2I.
 static qlin_status check_glu_shape(int64_t M, int64_t K, int64_t I) {
@@ -138,8 +144,9 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
       static const char *names[3] = {"k_quantize_act_i8bf16+k_w8_dq<16,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<32,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<64,i8>"};
+      static const char *fused[3] = {"k_w8_dq<16,i8,xq>", "k_w8_dq<32,i8,xq>", "k_w8_dq<64,i8,xq>"};
       const int b = i8_swap_bnt(M);
-      return names[b == 16 ? 0 : b == 32 ? 1 : 2];
+      return (i8_fused_quant(M) ? fused : names)[b == 16 ? 0 : b == 32 ? 1 : 2];
     }
   }
   return "invalid";
@@ -253,6 +260,7 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
     if (launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
     return from_cuda(launch_fp8_gemm(g, *dev, st));
   }
+  if (i8_fused_quant(M)) return from_cuda(launch_i8_swap(g, x, false, *dev, st, true));
   if (launch_quantize_act_i8bf16(M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
   return from_cuda(launch_i8_swap(g, ws, false, *dev, st));
 }
@@ -345,6 +353,7 @@ qlin_status qlin_w8a8_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int64
     if (launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
     return from_cuda(launch_fp8_gemm(g, *dev, st));
   }
+  if (i8_fused_quant(M)) return from_cuda(launch_i8_swap(g, x, false, *dev, st, true));
   if (launch_quantize_act_i8bf16(M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
   return from_cuda(launch_i8_swap(g, ws, false, *dev, st));
 }
