@@ -414,17 +414,22 @@ __device__ __forceinline__ void convert16(uint4 raw, uint32_t *o) {
       o[2 * i + 1] = pack_bf16x2(f2, f3);
     }
   } else {
-    // E4M3 pair -> f16x2 (exact) -> fp32 -> BF16 (exact: every E4M3 value is a BF16 value).
+    // E4M3 code s.eeee.mmm -> BF16 with the sign at bit 15 and eeee.mmm at bits
+    // 4..10: that BF16 number is the code's value times 2^-120 (a normal code has
+    // BF16 exponent field eeee and mantissa mmm/8; a subnormal code 0.mmm * 2^-6
+    // becomes the BF16 subnormal mmm * 2^-129), so one exact BF16 multiply by
+    // 2^120 gives the value.  Integer and FMA-pipe instructions only.
+    const __nv_bfloat162 k2p120 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x7B80),
+                                                     __ushort_as_bfloat16((unsigned short)0x7B80));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const unsigned short pair = (unsigned short)(w[i] >> (16 * h));
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-        __half2 hv = *reinterpret_cast<__half2 *>(&h2);
-        const float2 f = __half22float2(hv);
-        o[2 * i + h] = pack_bf16x2(f.x, f.y);
+        // codes 2h, 2h+1 of the word into the high bytes of the two 16-bit halves
+        const uint32_t t = __byte_perm(w[i], 0u, h ? 0x3424u : 0x1404u);
+        const uint32_t b = ((t >> 4) & 0x07F007F0u) | (t & 0x80008000u);
+        const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&b), k2p120);
+        o[2 * i + h] = *reinterpret_cast<const uint32_t *>(&v);
       }
     }
   }

@@ -260,3 +260,29 @@ def test_i8_gemm_multicast_bitexact(capi, M, K, N):
     qw = rng.integers(-127, 128, (N, K), dtype=np.int8)
     acc = capi.i8_gemm_s32(to_dev(qx.view(np.uint8)), to_dev(qw.view(np.uint8))).cpu().numpy()
     assert np.array_equal(acc, oracle.i8_gemm(qx, qw))
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+def test_w8a16_reads_every_weight_code_exactly(capi, qt):
+    """Every 8-bit weight code, including the E4M3 subnormals, negative zero and the
+    saturation codes, through the W8A16 linear: with one-hot activations and unit
+    scales, y[m, n] is the exact value of code q[n, m] (each is a BF16 number)."""
+    codes = np.array([c for c in range(256) if qt == "int8" or (c & 0x7F) != 0x7F], np.uint8)
+    if qt == "int8":
+        codes = codes[codes != 0x80]  # -128 is never produced
+    N = 256
+    K = int(np.ceil(len(codes) / 16.0) * 16)
+    q = np.zeros((N, K), np.uint8)
+    rng = np.random.default_rng(9)
+    for n in range(N):
+        q[n, :len(codes)] = rng.permutation(codes)
+    M = K
+    x = synth.f32_to_bf16_bits(np.eye(M, K, dtype=np.float32))  # token m selects column m
+    s = np.ones(N, np.float32)
+    y = synth.bf16_bits_to_f32(run_w8a16(capi, qt, x, q, s, None)).astype(np.float64)
+    if qt == "int8":
+        want = q.view(np.int8).astype(np.float64).T
+    else:
+        table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+        want = table[q].T
+    assert np.array_equal(y, want[:M]), int((y != want[:M]).sum())
