@@ -249,6 +249,13 @@ class GpuWorkload:
             self.ws.append(shared[("ws",) + shape_key])
             if len(cache) > 8:
                 cache.clear()
+        self.packed = not self.device_gen
+        if self.packed:
+            # one device buffer (and one pinned host mirror) for all of a step's
+            # activations, and one for all of its outputs: the end-to-end step
+            # moves each with a single copy, as a caller batching a step would
+            self.x, self.x_flat, self.x_host_flat = self._pack(self.x, dev, fill=True)
+            self.y, self.y_flat, self.y_host_flat = self._pack(self.y, dev, fill=False)
         torch.cuda.synchronize()
         P = ctypes.c_void_p
 
@@ -283,6 +290,26 @@ class GpuWorkload:
         self.kernel = [capi.qlin_kernel_name(op[l.form], l.qtype, l.M, l.K, l.N) for l in self.lins]
         self.set_accounting()
 
+    def _pack(self, tensors, dev, fill):
+        """Views of one 256-byte-aligned device buffer replacing `tensors` (their
+        contents copied when `fill`), plus a pinned host buffer of the same layout."""
+        torch = self.torch
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        flat = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+        host = torch.empty(max(total, 256), dtype=torch.uint8).pin_memory()
+        views = []
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            v = flat[o:o + n].view(t.dtype).view(t.shape)
+            if fill:
+                v.copy_(t)
+                host[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            views.append(v)
+        return views, flat, host
+
     def set_accounting(self):
         """Per-call algorithmic bytes / flops, the tensor peak each call is bound by,
         a description of each call, and the host<->device copies of the e2e step."""
@@ -291,8 +318,12 @@ class GpuWorkload:
         self.call_fp8 = [l.form == "w8a8" and l.qtype == "e4m3" for l in self.lins]
         self.call_info = [{"name": l.name, "M": l.M, "K": l.K, "N": l.N, **({"out": out_cols(l)} if l.glu else {})}
                           for l in self.lins]
-        self.h2d = [(self.x[i], self.x_host[i]) for i in range(len(self.lins))]
-        self.d2h = [(self.y_host[i], self.y[i]) for i in range(len(self.lins))]
+        if self.packed:
+            self.h2d = [(self.x_flat, self.x_host_flat)]
+            self.d2h = [(self.y_host_flat, self.y_flat)]
+        else:
+            self.h2d = [(self.x[i], self.x_host[i]) for i in range(len(self.lins))]
+            self.d2h = [(self.y_host[i], self.y[i]) for i in range(len(self.lins))]
         l0 = self.lins[0]
         self.dtype = (("e4m3" if l0.qtype == "e4m3" else "int8") + ("xbf16" if l0.form == "w8a16" else "")
                       + "->f32acc->bf16")
@@ -385,6 +416,7 @@ class KvWorkload(GpuWorkload):
         self.torch, self.capi = torch, capi
         self.name, self.dev, self.copies = name, dev, 1
         self.lins, self.wl = [], synth.KV7B
+        self.packed = False
         L = capi.lib()
         H, D, S, T = synth.KV_HEADS, synth.KV_HEAD_DIM, synth.KV_CONTEXT, synth.KV_CHUNK
         self.stream = torch.cuda.current_stream()
