@@ -714,13 +714,22 @@ __global__ void __launch_bounds__(640, 1)
     auto emit16 = [&](int m0, int c, int ochan, const float (&v)[16]) -> bool {
       uint16_t *y = (uint16_t *)p.y;
       if (!p.glu) {
-        if (ochan < p.N) {
+        // Transpose through this warp's 1 KB of the exchange area (two slots): each
+        // thread writes its channel for the 16 tokens, then lane l stores 8
+        // consecutive channels of token row (l / 4) and (l / 4) + 8 as one 16-byte
+        // vector.  N is a multiple of 16, so a chunk of 8 channels is all in or out.
+        uint16_t *stg = reinterpret_cast<uint16_t *>(xchg) + (q4 * 2 + (xround++ & 1)) * 16 * 32;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int m = m0 + c + e;
-            if (m < p.M) y[(size_t)m * p.N + ochan] = f32_to_bf16_bits(v[e]);
-          }
+        for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = f32_to_bf16_bits(v[e]);
+        __syncwarp();
+        const int ch = ochan - lane + (lane & 3) * 8;  // the warp's first channel + this lane's chunk
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = (lane >> 2) + 8 * h, m = m0 + c + r;
+          const uint4 vec = *reinterpret_cast<const uint4 *>(stg + r * 32 + (lane & 3) * 8);
+          if (m < p.M && ch < p.N) *reinterpret_cast<uint4 *>(y + (size_t)m * p.N + ch) = vec;
         }
+        __syncwarp();
         return true;
       }
       const int k = xround++, slot = k & 1, use = k >> 1;  // use: how often this slot was used before
@@ -777,16 +786,48 @@ __global__ void __launch_bounds__(640, 1)
         const uint32_t dt = tmem + lane_base + db * C::DSTRIDE;
         const int in_chunk = min(CH, nkb - ch * CH);
         const int nacc = in_chunk < C::NACC ? in_chunk : C::NACC;  // accumulators written in this chunk
-        // 16 columns of the chunk's sum: accumulators added in a fixed order
+        // 16 columns of the chunk's sum: accumulators added in a fixed order (all
+        // of a chunk's tensor-memory loads are issued before the one wait)
         auto load16 = [&](int c, uint32_t (&r)[16]) {
-          tmem_ld16(dt + c, r);
-          tmem_ld_wait();
-          for (int a = 1; a < nacc; ++a) {
-            uint32_t t[16];
-            tmem_ld16(dt + a * BNT + c, t);
+          if constexpr (C::NACC == 1) {
+            tmem_ld16(dt + c, r);
             tmem_ld_wait();
+          } else if constexpr (C::NACC > 2) {
+            // four small accumulators (16/32-token tiles, a short epilogue): one at a time
+            tmem_ld16(dt + c, r);
+            tmem_ld_wait();
+            for (int a = 1; a < nacc; ++a) {
+              uint32_t t[16];
+              tmem_ld16(dt + a * BNT + c, t);
+              tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(t[e]));
+              for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(t[e]));
+            }
+          } else {
+            // two accumulators: both loads in flight per wait
+            uint32_t t[16];
+            tmem_ld16(dt + c, r);
+            if (nacc > 1) tmem_ld16(dt + BNT + c, t);
+            tmem_ld_wait();
+            if (nacc > 1) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(t[e]));
+            }
+#pragma unroll
+            for (int a = 2; a < C::NACC; a += 2) {
+              if (a < nacc) {
+                uint32_t u[16];
+                tmem_ld16(dt + a * BNT + c, t);
+                if (a + 1 < nacc) tmem_ld16(dt + (a + 1) * BNT + c, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(t[e]));
+                if (a + 1 < nacc) {
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(u[e]));
+                }
+              }
+            }
           }
         };
         if constexpr (kI8) {
@@ -804,14 +845,36 @@ __global__ void __launch_bounds__(640, 1)
         } else if (S == 1) {
           const float sw = valid ? __ldg(p.w_scale + wrow) : 0.0f;
           const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + wrow)) : 0.0f;
+          if constexpr (C::NACC == 1) {
+            // double-buffered: the next 16 columns are loaded while these are stored
+            uint32_t ra[16], rb[16];
+            tmem_ld16(dt, ra);
 #pragma unroll 1
-          for (int c = 0; c < BNT && ok; c += 16) {
-            uint32_t r[16];
-            load16(c, r);
-            float v[16];
+            for (int c = 0; c < BNT && ok; c += 32) {
+              tmem_ld_wait();
+              if (c + 16 < BNT) tmem_ld16(dt + c + 16, rb);
+              float v[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = fmaf(__uint_as_float(r[e]), sw, b);
-            ok = emit16(m0, c, ochan, v);
+              for (int e = 0; e < 16; ++e) v[e] = fmaf(__uint_as_float(ra[e]), sw, b);
+              ok = emit16(m0, c, ochan, v);
+              if (c + 16 >= BNT) break;
+              tmem_ld_wait();
+              if (c + 32 < BNT) tmem_ld16(dt + c + 32, ra);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = fmaf(__uint_as_float(rb[e]), sw, b);
+              ok = ok && emit16(m0, c + 16, ochan, v);
+            }
+            tmem_ld_wait();  // no load left in flight past the accumulator release
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < BNT && ok; c += 16) {
+              uint32_t r[16];
+              load16(c, r);
+              float v[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = fmaf(__uint_as_float(r[e]), sw, b);
+              ok = emit16(m0, c, ochan, v);
+            }
           }
         } else {
           uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // partial tile, [token][channel]
