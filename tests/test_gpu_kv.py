@@ -78,7 +78,7 @@ def _compare_cache(gc, oc):
 
 
 @pytest.mark.parametrize("D", [32, 64, 128, 256])
-@pytest.mark.parametrize("H,T", [(1, 1), (2, 37), (4, 300), (8, 1029)])
+@pytest.mark.parametrize("H,T", [(1, 1), (2, 37), (3, 64), (4, 300), (5, 33), (6, 129), (8, 1029)])
 def test_kv_store_and_load_bit_exact(capi, orc, D, H, T):
     S = T + 64
     k, v = _inputs(T, H, D, "a")
