@@ -77,6 +77,78 @@ __device__ __forceinline__ uint8_t quantize_one(float x, const Scale &c) {
   }
 }
 
+// ------------------------------------------------ static E4M3, eight at a time
+// The static E4M3 quantizer of a whole tensor (one run-time scale s) gives the
+// same codes as quantize_one<QLIN_E4M3, false> for every finite input, with
+// about half the instructions, which matters where the conversion shares an SM
+// with a GEMM:
+//   - |x| is first clamped to B, the smallest BF16 >= 512 s, two lanes at a time
+//     on the packed BF16 input (min of absolute values, sign kept).  Every
+//     |x| >= B has |x/s| >= 512 > 448 and saturates to +-448 either way, and
+//     after the clamp x * r cannot overflow, so the quotient needs no clamp.
+//   - The quotient's multiply and two FMAs run as packed f32x2 operations
+//     (the same IEEE round-to-nearest operations, lane by lane).
+//   - The sign of x is ORed into each code byte: for x != 0 the code already
+//     carries it, and for x = -0 the correction step returns +0 and the OR
+//     restores -0's code 0x80 (what the copysign of quotient() does).
+// Off the fast scale range it is quantize_one itself, element by element.
+struct StaticE4m3 {
+  Scale c;
+  uint32_t bound2;   // B in both BF16 halves
+  uint64_t r2, ns2;  // (r, r) and (-s, -s) as f32x2
+};
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ StaticE4m3 make_static_e4m3(float s) {
+  StaticE4m3 q;
+  q.c = make_scale(s);
+  uint32_t b = 0x7F80u;  // +inf
+  if (q.c.fast) {
+    const uint32_t bits = __float_as_uint(512.0f * s);  // exact (s <= 2^96)
+    b = (bits >> 16) + ((bits & 0xFFFFu) ? 1u : 0u);    // round up to BF16
+  }
+  q.bound2 = b | (b << 16);
+  q.r2 = f32x2_pack(q.c.r, q.c.r);
+  q.ns2 = f32x2_pack(-s, -s);
+  return q;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Two BF16 (one word) -> two E4M3 codes in the low 16 bits (lane 0 in byte 0);
+// fast scale range only, sign of a zero not yet restored.
+__device__ __forceinline__ uint32_t e4m3_static2_fast(uint32_t w, const StaticE4m3 &q) {
+  uint32_t wc;
+  asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(wc) : "r"(w), "r"(q.bound2));
+  const uint64_t x = f32x2_pack(__uint_as_float(wc << 16), __uint_as_float(wc & 0xFFFF0000u));
+  const uint64_t q0 = f32x2_mul(x, q.r2);
+  const uint64_t rem = f32x2_fma(q0, q.ns2, x);
+  const uint64_t q1 = f32x2_fma(rem, q.r2, q0);
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(
+      make_float2(__uint_as_float((uint32_t)q1), __uint_as_float((uint32_t)(q1 >> 32))), __NV_SATFINITE,
+      __NV_E4M3);
+}
+// Four BF16 (two words) -> four codes, element i in byte i.  The _fast form
+// (no branch, so a caller's unrolled loop schedules freely) needs q.c.fast.
+__device__ __forceinline__ uint32_t e4m3_static4_fast(uint32_t w0, uint32_t w1, const StaticE4m3 &q) {
+  const uint32_t c = __byte_perm(e4m3_static2_fast(w0, q), e4m3_static2_fast(w1, q), 0x5410);
+  return c | (__byte_perm(w0, w1, 0x7531) & 0x80808080u);  // the BF16 sign bits
+}
+__device__ __forceinline__ uint32_t e4m3_static4_exact_div(uint32_t w0, uint32_t w1, const Scale &c) {
+  return (uint32_t)quantize_one<QLIN_E4M3, false>(bf16_bits_to_f32(w0 & 0xFFFFu), c) |
+         ((uint32_t)quantize_one<QLIN_E4M3, false>(bf16_bits_to_f32(w0 >> 16), c) << 8) |
+         ((uint32_t)quantize_one<QLIN_E4M3, false>(bf16_bits_to_f32(w1 & 0xFFFFu), c) << 16) |
+         ((uint32_t)quantize_one<QLIN_E4M3, false>(bf16_bits_to_f32(w1 >> 16), c) << 24);
+}
+
 // Exact value of an 8-bit code as fp32 (every INT8 / E4M3 value is exact in fp32).
 template <int QT>
 __device__ __forceinline__ float code_to_f32(uint8_t c) {

@@ -85,6 +85,15 @@ struct Fp8Params {
   int mtiles, ntiles;
   int xs_per_token;  // x_scale holds one scale per token row
   int glu;           // merged gate_up: B tile = 128 gate rows + the matching 128 up rows
+  // Fused static quantization (XQ): warps 2-3 of every CTA quantize the BF16
+  // activations (read through tm_x) into the codes xq_dst that tm_a reads, one
+  // task per (m-tile, 128-k block); a task's flag (xq_flags, row stride
+  // xq_fstride) becomes 1 when all of its codes are written, and the
+  // count of band b (xq_flags[mtiles * xq_fstride + b]) counts its finished tasks.  Tasks run
+  // in bands of xq_band m-tiles, k-major inside a band.
+  uint8_t *xq_dst;
+  unsigned *xq_flags;
+  int xq_fstride, xq_band;
   const float *w_scale;
   const float *x_scale;
   const uint16_t *bias;
@@ -92,25 +101,56 @@ struct Fp8Params {
   unsigned *status;
 };
 
-struct Fp8Cfg {
-  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+// XQ roles of the 512-thread variant: warp 2 stages BF16 chunks (TMA), warps
+// 12..15 convert them, warp 3 publishes finished tasks.
+constexpr int kXqConverters = 4;
+constexpr int kXqPrefetch = 0;  // chunks brought into L2 ahead of the staging ring
+
+// GEMM pipeline depth of the fused-quantization variant (a stage given up
+// there, 48 KB, would buy the quantizer three more chunks of staging).
+constexpr int kFp8XqStages = 4;
+
+template <int XQ>
+struct Fp8CfgT {
+  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages : 4;
   static constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;
-  static constexpr int THREADS = 384;
+  // XQ: a ring of chunks (64 rows of a task's 128 x 128 BF16 activation tile),
+  // TMA-staged, as many as the rest of the shared memory holds
+  static constexpr int XQ_CHUNK = (BM / 2) * BK * 2, XQ_OFF = BAR_OFF + 256;
+  static constexpr int XQ_NBUF = XQ ? (227 * 1024 - XQ_OFF - 1024) / XQ_CHUNK : 0;
+  static constexpr int SMEM = XQ_OFF + XQ_NBUF * XQ_CHUNK + 1024;
+  static constexpr int THREADS = XQ ? 512 : 384;
   static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, BN);
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(XQ == 0 || (XQ_NBUF >= 2 && XQ_NBUF <= 6), "chunk ring (barriers and counters at BAR_OFF + 128)");
 };
+using Fp8Cfg = Fp8CfgT<0>;
 
 // MC = 2: the CTAs of a 2-CTA cluster take the two m-tiles of a pair with the
 // same n-tile; each loads its own A tile and half of the shared B tile, which
 // TMA multicasts into both CTAs, so every B byte leaves L2 once per pair.  A
 // stage may be refilled only when both CTAs' MMAs have read it: the MMA
 // commits arrive on the stage's empty barrier in both CTAs.
-template <int MC>
-__global__ void __launch_bounds__(384, 1)
-    k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, Fp8Params p) {
-  using C = Fp8Cfg;
+//
+// XQ = 1: the activations are quantized inside the kernel.  Warps 2-3 and
+// 12-15 (a 512-thread block) of every CTA take quantization tasks (m-tile,
+// 128-k block).  TMA streams each task's BF16 tile into a ring of 64-row chunks
+// in shared memory, several tasks ahead; the warps write the E4M3 codes to
+// global memory and release the task's flag and its band's count.  Tasks go in
+// bands of m-tiles about one wave of GEMM tiles wide, k-major inside a band, so
+// the first k-blocks of every tile of a wave are ready first.  The TMA producer
+// loads a tile with no checks once it has seen the tile's band (and all before
+// it) complete; otherwise it acquires a group of four task flags (the next
+// group's load already in flight) before loading those A tiles, and fences the
+// async proxy after either acquire.  The quantization streams from HBM while
+// the GEMM is bound by the tensor cores and L2, so it overlaps.  The launch is
+// cooperative: every CTA is resident, and every wait is bounded besides.
+template <int MC, int XQ>
+__global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
+    k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_x, Fp8Params p) {
+  using C = Fp8CfgT<XQ>;
   static_assert(MC == 1 || MC == 2, "cluster of one or two CTAs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -142,6 +182,16 @@ __global__ void __launch_bounds__(384, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+    if constexpr (XQ == 1) {
+      uint64_t *xq_full = (uint64_t *)(smem + C::BAR_OFF + 128), *xq_empty = xq_full + C::XQ_NBUF;
+      unsigned *xq_count = (unsigned *)(xq_empty + C::XQ_NBUF);
+      for (int b = 0; b < C::XQ_NBUF; ++b) {
+        mbar_init(&xq_full[b], 1);
+        mbar_init(&xq_empty[b], kXqConverters);
+      }
+      for (int w = 0; w < kXqConverters; ++w) xq_count[w] = 0;
+      tma_prefetch_desc(&tm_x);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
@@ -155,11 +205,58 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {  // ------------------------------- TMA producer
     if (lane == 0) {
       int i = 0;
+      // XQ: the tiles of bands 0..ready_band (seen complete, fenced once) load
+      // with no flag checks; the others check the flags of each group of four
+      // k-blocks, the next group's flags loaded one group ahead.
+      auto group_flags = [&](int t, int g) { return p.xq_flags + (tile_m0(t) / C::BM) * p.xq_fstride + 4 * g; };
+      const unsigned *band_done = p.xq_flags + p.mtiles * p.xq_fstride;
+      int ready_band = -1;
+      uint4 pf = make_uint4(0, 0, 0, 0);
       for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
         const int t = cid + j * G;
         const int m0 = tile_m0(t), n0 = tile_n0(t);
+        bool tile_ready = true;  // also for the empty second m-tile of a pair past M (no codes)
+        if constexpr (XQ == 1) {
+          const int band = (m0 / C::BM) / p.xq_band;
+          if (m0 < p.M && band > ready_band) {
+            pf = ld_relaxed_v4(group_flags(t, 0));  // in flight while the band counters are read
+            int b = ready_band + 1;
+            while (b <= band &&
+                   ld_relaxed_u32(band_done + b) >= (unsigned)(min(p.xq_band, p.mtiles - b * p.xq_band) * nkb))
+              ++b;
+            if (b > ready_band + 1) {
+              fence_acq_rel_gpu();         // acquire: every code of those bands is written
+              fence_proxy_async_global();  // ... before this thread's TMA reads of them
+              ready_band = b - 1;
+            }
+            tile_ready = band <= ready_band;
+          }
+        }
         for (int kb = 0; kb < nkb; ++kb, ++i) {
           const int s = i % C::STAGES;
+          if constexpr (XQ == 1) {
+            if (!tile_ready && (kb & 3) == 0) {
+              uint4 cur = pf;
+              if (kb + 4 < nkb) pf = ld_relaxed_v4(group_flags(t, kb / 4 + 1));  // the next group
+              const int need = min(4, nkb - kb);  // flags of k-blocks past K are never set
+              auto ready = [&](uint4 v) {
+                return v.x != 0u && (need < 2 || v.y != 0u) && (need < 3 || v.z != 0u) && (need < 4 || v.w != 0u);
+              };
+              if (!ready(cur)) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!ready(cur = ld_relaxed_v4(group_flags(t, kb / 4)))) {
+                  if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    break;
+                  }
+                  __nanosleep(64);
+                }
+                if (*abort_flag) break;
+              }
+              fence_acq_rel_gpu();         // acquire: the task's code writes happen before what follows
+              fence_proxy_async_global();  // ... including this thread's TMA reads of them
+            }
+          }
           if (i >= C::STAGES && !mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
             *abort_flag = 1;
             break;
@@ -176,6 +273,131 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, b0);
             tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, b1);
           }
+        }
+      }
+    }
+  } else if (XQ == 1 && (warp == 2 || warp == 3 || warp >= 12)) {  // ----- activation quantizer
+    uint64_t *xq_full = (uint64_t *)(smem + C::BAR_OFF + 128), *xq_empty = xq_full + C::XQ_NBUF;
+    unsigned *xq_count = (unsigned *)(xq_empty + C::XQ_NBUF);  // tasks finished, per converter warp
+    const uint8_t *xq_buf = smem + C::XQ_OFF;
+    const int tasks = p.mtiles * nkb, per_band = p.xq_band * nkb;
+    const int mine = (int)blockIdx.x < tasks ? (tasks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    auto task_of = [&](int j, int &mt, int &kb) {
+      const int u = (int)blockIdx.x + j * (int)gridDim.x, band = u / per_band, r = u - band * per_band;
+      const int nb = min(p.xq_band, p.mtiles - band * p.xq_band);  // the last band may be narrower
+      kb = r / nb;
+      mt = band * p.xq_band + (r - kb * nb);
+    };
+    // chunk c = half c & 1 of task c >> 1 goes through ring buffer c % NB
+    constexpr int NB = C::XQ_NBUF;
+    const int chunks = 2 * mine;
+    if (warp == 2) {  // ---- staging: TMA loads of BF16 chunks into the ring
+      if (lane == 0) {
+        // chunks kXqPrefetch ahead of the one being loaded are brought into L2,
+        // so the ring's loads see L2 latency rather than HBM latency
+        auto prefetch = [&](int c) {
+          if (c >= chunks) return;
+          int mt, kb;
+          task_of(c >> 1, mt, kb);
+          tma_prefetch_l2_2d(&tm_x, kb * C::BK, mt * C::BM + (c & 1) * (C::BM / 2));
+        };
+        for (int c = 0; c < kXqPrefetch; ++c) prefetch(c);
+        // the BF16 activations are read once: they must not push the GEMM's
+        // reused weight and code tiles out of L2
+        const uint64_t policy = l2_policy_evict_first();
+        int issued = 0;
+        bool ok = true;
+        for (; issued < chunks; ++issued) {
+          const int c = issued, b = c % NB;
+          if constexpr (kXqPrefetch > 0) prefetch(c + kXqPrefetch);
+          if (c >= NB && !mbar_wait(&xq_empty[b], (uint32_t)(c / NB - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          int mt, kb;
+          task_of(c >> 1, mt, kb);
+          mbar_arrive_expect_tx(&xq_full[b], C::XQ_CHUNK);
+          tma_load_2d_hint(&tm_x, &xq_full[b], (void *)(xq_buf + b * C::XQ_CHUNK), kb * C::BK,
+                           mt * C::BM + (c & 1) * (C::BM / 2), policy);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          // loads that may still be in flight land before the CTA leaves
+          for (int c = max(0, issued - NB); c < issued; ++c)
+            mbar_wait_drain(&xq_full[c % NB], (uint32_t)(c / NB) & 1);
+        }
+      }
+    } else if (warp == 3) {  // ---- publishing: flags and band counts of finished tasks
+      if (lane == 0) {
+        int released = 0;
+        while (released < mine) {
+          int done = 0;
+          const uint64_t t0 = globaltimer_ns();
+          while (true) {
+            done = mine;
+            for (int w = 0; w < kXqConverters; ++w) done = min(done, (int)ld_acquire_cta_shared(&xq_count[w]));
+            if (done > released || *abort_flag) break;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              *abort_flag = 1;
+              break;
+            }
+            __nanosleep(32);
+          }
+          if (done <= released) break;  // aborted
+          // one release for every task finished since the last: the acquire
+          // loads above saw all their code stores, and the fence is cumulative
+          fence_proxy_async_global();  // the codes are read through the async proxy (TMA)
+          fence_acq_rel_gpu();
+          for (; released < done; ++released) {
+            int mt, kb;
+            task_of(released, mt, kb);
+            red_relaxed_add_u32(p.xq_flags + mt * p.xq_fstride + kb, 1u);
+            red_relaxed_add_u32(p.xq_flags + p.mtiles * p.xq_fstride + mt / p.xq_band, 1u);
+          }
+        }
+      }
+    } else {  // ---- conversion: warps 12..15, 128 threads
+      const int qt = threadIdx.x - 384;
+      const StaticE4m3 xs = make_static_e4m3(__ldg(p.x_scale));
+      for (int c = 0; c < chunks; ++c) {
+        const int b = c % NB;
+        // the warp takes one path whatever each lane's bounded wait saw
+        if (!__all_sync(0xffffffffu, mbar_wait(&xq_full[b], (uint32_t)(c / NB) & 1, abort_flag))) {
+          *abort_flag = 1;
+          break;
+        }
+        int mt, kb;
+        task_of(c >> 1, mt, kb);
+        const uint32_t src = smem_u32(xq_buf + b * C::XQ_CHUNK);
+        const int mh = mt * C::BM + (c & 1) * (C::BM / 2), k0 = kb * C::BK;
+        // 64 rows x 16 pieces of 8 BF16 (16 consecutive threads cover one row's
+        // 256 bytes): each thread reads its eight pieces first, then converts
+        // and stores them, eight independent chains
+        constexpr int PIECES = (C::BM / 2) * 16 / (32 * kXqConverters);
+        static_assert(PIECES * 32 * kXqConverters == (C::BM / 2) * 16, "pieces per converter thread");
+        uint4 v[PIECES];
+#pragma unroll
+        for (int i = 0; i < PIECES; ++i) v[i] = lds128(src + 16u * (qt + i * 32 * kXqConverters));
+        uint2 q[PIECES];
+        if (xs.c.fast) {  // uniform: the branch stays outside the unrolled conversions
+#pragma unroll
+          for (int i = 0; i < PIECES; ++i)
+            q[i] = make_uint2(e4m3_static4_fast(v[i].x, v[i].y, xs), e4m3_static4_fast(v[i].z, v[i].w, xs));
+        } else {
+#pragma unroll
+          for (int i = 0; i < PIECES; ++i)
+            q[i] = make_uint2(e4m3_static4_exact_div(v[i].x, v[i].y, xs.c),
+                              e4m3_static4_exact_div(v[i].z, v[i].w, xs.c));
+        }
+#pragma unroll
+        for (int i = 0; i < PIECES; ++i) {
+          const int e = qt + i * 32 * kXqConverters, row = e >> 4, col = k0 + (e & 15) * 8;
+          if (mh + row < p.M && col < p.K) *reinterpret_cast<uint2 *>(p.xq_dst + (size_t)(mh + row) * p.K + col) = q[i];
+        }
+        __syncwarp();  // the warp's reads of the buffer and its code stores come before ...
+        if (lane == 0) {
+          mbar_arrive(&xq_empty[b]);                                             // ... the refill
+          if (c & 1) red_release_cta_shared_add(&xq_count[warp - 12], 1u);     // ... the publication
         }
       }
     }
@@ -1005,19 +1227,54 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   // glu: an output tile is 128 channels (n0 counts the 256 gate+up columns of the MMA tile)
   const int mtiles = (int)((g.M + C::BM - 1) / C::BM);
   const int ntiles = g.glu ? (int)(g.N / (C::BN / 2)) : (int)((g.N + C::BN - 1) / C::BN);
-  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.glu, g.w_scale, g.x_scale,
+  const int nkb = (int)((g.K + C::BK - 1) / C::BK);
+  Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.glu,
+              (uint8_t *)g.a, g.xq_flags, (nkb + 3) / 4 * 4, 1, g.w_scale, g.x_scale,
               g.bias, (uint16_t *)g.y, dev.status};
+  // band of quantization tasks: the m-tiles one wave of `slots` work items spans
+  auto band = [&](int slots, int mc) {
+    const int b = mc * ((slots + ntiles - 1) / ntiles);
+    return b < mtiles ? b : mtiles;
+  };
+  if (g.xq) {  // fused quantization: cooperative launch; pairs share B where clusters combine with it
+    if (g.x_scale_per_token || !g.xq_flags) return cudaErrorInvalidValue;
+    CUtensorMap tx;  // the BF16 activations, chunks of 64 rows of a 128 x 128 task tile
+    if (!make_map(&tx, g.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, C::BM / 2,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    const size_t fb = fp8_xq_flag_bytes(g.M, g.K);
+    cudaError_t e = cudaMemsetAsync(g.xq_flags, 0, fb, st);
+    if (e != cudaSuccess) return e;
+    using CX = Fp8CfgT<1>;
+    static cudaError_t a2 = set_smem(k_fp8_gemm<2, 1>, CX::SMEM);
+    static cudaError_t a1 = set_smem(k_fp8_gemm<1, 1>, CX::SMEM);
+    static bool pairs_ok = true;  // cleared if this device refuses cooperative cluster launches
+    if (mtiles >= 2 && pairs_ok && a2 == cudaSuccess) {
+      const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
+      const int grid = 2 * (items < pairs ? items : pairs);
+      p.xq_band = band(grid / 2, 2);
+      e = launch_kernel_coop(k_fp8_gemm<2, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 2, ta, tb,
+                             tx, p);
+      if (e == cudaSuccess) return e;
+      pairs_ok = false;
+    }
+    if (a1 != cudaSuccess) return a1;
+    const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
+    p.xq_band = band(grid, 1);
+    return launch_kernel_coop(k_fp8_gemm<1, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 1, ta, tb,
+                              tx, p);
+  }
   if (mtiles >= 2) {  // pairs of m-tiles share their B tiles (2-CTA clusters, TMA multicast)
-    static cudaError_t attr2 = set_smem(k_fp8_gemm<2>, C::SMEM);
+    static cudaError_t attr2 = set_smem(k_fp8_gemm<2, 0>, C::SMEM);
     if (attr2 != cudaSuccess) return attr2;
     const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
     const int grid = 2 * (items < pairs ? items : pairs);
-    return launch_kernel_x(k_fp8_gemm<2>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 2, ta, tb, p);
+    return launch_kernel_x(k_fp8_gemm<2, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 2, ta, tb, tb, p);
   }
-  static cudaError_t attr = set_smem(k_fp8_gemm<1>, C::SMEM);
+  static cudaError_t attr = set_smem(k_fp8_gemm<1, 0>, C::SMEM);
   if (attr != cudaSuccess) return attr;
   const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-  return launch_kernel(k_fp8_gemm<1>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, p);
+  return launch_kernel(k_fp8_gemm<1, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, p);
 }
 
 // Token tile (MMA N) of the W8A16 swap-AB kernel.  Up to 128 tokens the tile
@@ -1027,6 +1284,27 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
 // of each is estimated as waves x k-blocks per CTA x per-block cost, where a
 // 256-token block costs 1.63 times a 128-token block (the ratio of their
 // per-unit times measured on the 7B gate_up shape, K = 3584, N = 37888).
+// Task flags of the fused-quantization FP8 GEMM: one u32 per (m-tile, 128-k
+// block), each m-tile's row padded to a multiple of four (read four at a time),
+// then one u32 per band of m-tiles (at most one band per m-tile).
+size_t fp8_xq_flag_bytes(int64_t M, int64_t K) {
+  const int64_t mtiles = (M + Fp8Cfg::BM - 1) / Fp8Cfg::BM, nkb = (K + Fp8Cfg::BK - 1) / Fp8Cfg::BK;
+  return (size_t)(mtiles * ((nkb + 3) / 4 * 4 + 1) * 4);
+}
+
+// The fused kernel pays a start-up of one quantization task before the first
+// tiles can load, and its quantizer shares the SMs' shared-memory bandwidth
+// with the GEMM.  It wins where the activations are many (16 m-tiles and up)
+// and each GEMM row is short (at most 4096 columns, so the quantization is a
+// large share of the work); on wider GEMMs the separate quantization pass is as
+// fast or faster.  Its quantizers are the GEMM's CTAs, so the tile pairs must
+// fill every SM.  N counts GEMM columns (2I for the merged gate_up).
+bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms) {
+  (void)K;
+  const int64_t mtiles = (M + Fp8Cfg::BM - 1) / Fp8Cfg::BM, ntiles = (N + Fp8Cfg::BN - 1) / Fp8Cfg::BN;
+  return mtiles >= 16 && N <= 4096 && ((mtiles + 1) / 2) * ntiles >= sms / 2;
+}
+
 int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms) {
   if (M <= 128) return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   const int64_t kb = (K + 63) / 64, nt = (N + 127) / 128;

@@ -47,6 +47,35 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// A cooperative launch (every CTA resident at once, which the fused-quantization
+// GEMM's cross-CTA flags rely on), with an optional cluster shape along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               unsigned cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeCooperative;
+  attrs[na].val.cooperative = 1;
+  ++na;
+  if (cluster_x > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = cluster_x;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // As launch_kernel, with a cluster shape along x.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel_x(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -96,7 +125,16 @@ struct GemmArgs {
   void *y;                // [M,N] BF16, or int32 for kI8Raw
   int x_scale_per_token = 0;  // x_scale holds one scale per token row (dynamic W8A8)
   int glu = 0;  // merged gate_up: qw/w_scale/bias have 2N rows (gate rows first), y = silu(gate) * up [M, N]
+  // FP8 W8A8 with the static quantization inside the GEMM: `a` is the codes
+  // workspace, xq the BF16 activations, xq_flags the zeroed task flags
+  const void *xq = nullptr;
+  unsigned *xq_flags = nullptr;
 };
+
+// Fused-quantization FP8 GEMM: task-flag area (u32) for these sizes, and
+// whether the fused kernel is used.
+size_t fp8_xq_flag_bytes(int64_t M, int64_t K);
+bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms);
 
 // Mixed KV cache (kv_kernels.cu): INT8 keys with float16 group-32 scales,
 // E4M3 values with float16 per-(token, head) scales.

@@ -140,7 +140,7 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_W8A8_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
-      if (qtype == QLIN_E4M3) return "k_quantize_act+k_fp8_gemm";
+      if (qtype == QLIN_E4M3) return fp8_xq_used(M, K, N, sm_count()) ? "k_fp8_gemm<xq>" : "k_quantize_act+k_fp8_gemm";
       static const char *names[3] = {"k_quantize_act_i8bf16+k_w8_dq<16,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<32,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<64,i8>"};
@@ -171,8 +171,12 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     case QLIN_OP_ACT_SCALE: return 256;
     case QLIN_OP_QUANTIZE_ACT: return 0;
     case QLIN_OP_W8A16_LINEAR: return 0;
-    // quantized activations: E4M3 codes (1 byte), or INT8 codes as integer-valued BF16 (2 bytes)
-    case QLIN_OP_W8A8_LINEAR: return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256);
+    // quantized activations: E4M3 codes (1 byte) and, for the fused-quantization GEMM, its
+    // task flags; or INT8 codes as integer-valued BF16 (2 bytes)
+    case QLIN_OP_W8A8_LINEAR:
+    case QLIN_OP_W8A8_GATE_UP_SILU:
+      if (qtype == QLIN_E4M3) return round_up((size_t)M * (size_t)K, 256) + round_up(fp8_xq_flag_bytes(M, K), 256);
+      return round_up((size_t)M * (size_t)K * 2, 256);
     case QLIN_OP_I8_GEMM_S32: return round_up((size_t)M * (size_t)K * 2, 256);
     // per-token codes (as for the static path) followed by the per-token scales
     case QLIN_OP_W8A8_DYNAMIC_LINEAR:
@@ -181,8 +185,6 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     case QLIN_OP_KV_LOAD_MIXED:
     case QLIN_OP_W8A16_GATE_UP_SILU:
       return 0;
-    case QLIN_OP_W8A8_GATE_UP_SILU:
-      return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256);
   }
   return (size_t)-1;
 }
@@ -257,6 +259,11 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
   cudaStream_t st = (cudaStream_t)stream;
   GemmArgs g{kW8A8, qtype, M, K, N, ws, qw, w_scale, input_scale, (const uint16_t *)bias, y};
   if (qtype == QLIN_E4M3) {
+    if (fp8_xq_used(M, K, g.N, dev->sms)) {  // one kernel: quantization overlapped with the GEMM
+      g.xq = x;
+      g.xq_flags = (unsigned *)((char *)ws + round_up((size_t)M * (size_t)K, 256));
+      return from_cuda(launch_fp8_gemm(g, *dev, st));
+    }
     if (launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
     return from_cuda(launch_fp8_gemm(g, *dev, st));
   }
@@ -350,6 +357,11 @@ qlin_status qlin_w8a8_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int64
   GemmArgs g{kW8A8, qtype, M, K, I, ws, qw, w_scale, input_scale, (const uint16_t *)bias, y};
   g.glu = 1;
   if (qtype == QLIN_E4M3) {
+    if (fp8_xq_used(M, K, 2 * g.N, dev->sms)) {  // one kernel: quantization overlapped with the GEMM
+      g.xq = x;
+      g.xq_flags = (unsigned *)((char *)ws + round_up((size_t)M * (size_t)K, 256));
+      return from_cuda(launch_fp8_gemm(g, *dev, st));
+    }
     if (launch_quantize_act(qtype, M, K, x, input_scale, ws, dev->sms, st) != cudaSuccess) return QLIN_ERR_CUDA;
     return from_cuda(launch_fp8_gemm(g, *dev, st));
   }

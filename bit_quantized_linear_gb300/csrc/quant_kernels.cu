@@ -93,6 +93,7 @@ __global__ void k_scale_finalize(const unsigned *__restrict__ amax_bits, float *
 // ---------------------------------------------------------------------------
 // Static activation quantization: 16 BF16 in (two 16-byte loads), 16 codes out
 // (one 16-byte store) per thread step.  The scale is read from device memory.
+// E4M3 on the fast scale range takes the packed form of the same arithmetic.
 // ---------------------------------------------------------------------------
 template <int QT>
 __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ x,
@@ -100,7 +101,20 @@ __global__ void __launch_bounds__(256) k_quantize_act(const uint4 *__restrict__ 
                                                       uint4 *__restrict__ q, int64_t n16) {
   pdl_wait();
   pdl_trigger();
-  const Scale s = make_scale(__ldg(s_ptr));
+  const float sv = __ldg(s_ptr);
+  const Scale s = make_scale(sv);
+  if constexpr (QT == QLIN_E4M3) {
+    if (s.fast) {
+      const StaticE4m3 se = make_static_e4m3(sv);
+      for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+           i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 a = __ldg(x + 2 * i), b = __ldg(x + 2 * i + 1);
+        q[i] = make_uint4(e4m3_static4_fast(a.x, a.y, se), e4m3_static4_fast(a.z, a.w, se),
+                          e4m3_static4_fast(b.x, b.y, se), e4m3_static4_fast(b.z, b.w, se));
+      }
+      return;
+    }
+  }
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
        i += (int64_t)gridDim.x * blockDim.x) {
     uint4 a = __ldg(x + 2 * i), b = __ldg(x + 2 * i + 1);

@@ -104,6 +104,13 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A8_GATE_UP_SILU, "e4m3", 4, 64, 128) >= 256
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_GATE_UP_SILU, 0, 1, 3584, 18944) == "k_w8_dq<16>"
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 11008) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 2048) == "k_fp8_gemm<xq>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 4096) == "k_fp8_gemm<xq>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 4112) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 1920, 2048, 2048) == "k_quantize_act+k_fp8_gemm"
+    # one n-tile: the pairs would not fill the SMs
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 256) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 1024, 2048, 11008) == "k_quantize_act+k_fp8_gemm"
 
 
 def test_no_device_is_reported_not_crashed(capi):

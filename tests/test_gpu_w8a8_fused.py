@@ -83,3 +83,78 @@ def test_fused_int8_gate_up_silu(capi):
     assert capi.qlin_get_device_status() == capi.QLIN_OK
     ref = oracle.w8a8_gate_up_silu(oracle.INT8, oracle.quantize_act(oracle.INT8, x, sx), sx, q, s)
     check_tol(from_dev_bf16(y), ref, "fused int8 gate_up silu")
+
+
+# ---------------------------------------------------------------- FP8 (E4M3)
+# From 16 token tiles (M > 1920), for GEMMs of at most 4096 columns whose tile
+# pairs fill the SMs, the E4M3 W8A8 linear is one kernel too: warps of every
+# GEMM CTA quantize the activations into the codes workspace, task by task, and
+# the TMA producer waits on each task's flag (or its band's count) before
+# loading those codes, so the quantization overlaps the tensor-core work.
+
+def _run_e4m3(capi, M, K, N, tag, x_scale_mult=1.0, with_bias=False, glu=False):
+    rng = synth.rng_for("test-w8a8-fused", 0, f"e4m3-{M}x{K}x{N}-{tag}", "all")
+    outl = synth.outlier_channels(K, rng)
+    rows_w = 2 * N if glu else N
+    w = synth.weights(rows_w, K, rng)
+    cal = synth.activations(512, K, rng, outl)
+    x = synth.activations(M, K, rng, outl)
+    if x_scale_mult != 1.0:
+        x = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x) * np.float32(x_scale_mult))
+    b = synth.bias(rows_w, rng) if with_bias else None
+    q, s = oracle.quantize_weight(oracle.E4M3, w)
+    sx = oracle.act_scale(oracle.E4M3, cal)
+    op = capi.QLIN_OP_W8A8_GATE_UP_SILU if glu else capi.QLIN_OP_W8A8_LINEAR
+    assert capi.qlin_kernel_name(op, "e4m3", M, K, N) == "k_fp8_gemm<xq>"
+    fn = capi.w8a8_gate_up_silu if glu else capi.w8a8_linear
+    y = fn("e4m3", to_dev_bf16(x), to_dev(np.array([sx], np.float32)), to_dev(q), to_dev(s),
+           None if b is None else to_dev_bf16(b))
+    torch.cuda.synchronize()
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 24)), [M - 1]]))
+    qx = oracle.quantize_act(oracle.E4M3, x, sx)
+    ref = (oracle.w8a8_gate_up_silu if glu else oracle.w8a8)(oracle.E4M3, qx, sx, q, s, b, rows=rows)
+    check_tol(from_dev_bf16(y)[rows], ref, f"fused e4m3 {M}x{K}x{N} {tag}")
+
+
+@pytest.mark.parametrize("M,K,N", [(2560, 2048, 2048), (2561, 1024, 2304), (2600, 2064, 2048), (4096, 16, 2560),
+                                   (2560, 11008, 2048)])
+def test_fused_e4m3_w8a8_shapes(capi, M, K, N):
+    _run_e4m3(capi, M, K, N, "shapes", with_bias=(K % 128 != 0))
+
+
+def test_fused_e4m3_w8a8_beyond_calibration_range(capi):
+    _run_e4m3(capi, 2304, 1024, 4096, "clamp", x_scale_mult=40.0)
+
+
+def test_fused_e4m3_gate_up_silu(capi):
+    _run_e4m3(capi, 2560, 2048, 1024, "glu", glu=True, with_bias=True)
+
+
+@pytest.mark.parametrize("M,K,N", [(2433, 2064, 2048), (4096, 16, 2048), (2400, 1040, 4096)])
+def test_fused_e4m3_codes_bitexact(capi, M, K, N):
+    """The in-GEMM quantizer leaves its codes in the workspace's first M*K bytes:
+    they must equal the oracle's static E4M3 quantization bit for bit, here with
+    signed zeros and values far beyond the calibration range mixed in."""
+    rng = synth.rng_for("test-w8a8-fused", 0, f"e4m3-codes-{M}x{K}", "all")
+    x = synth.activations(M, K, rng, synth.outlier_channels(K, rng))
+    xf = synth.bf16_bits_to_f32(x)
+    pick = rng.random(xf.shape)
+    xf = np.where(pick < 0.01, np.float32(-0.0), xf)
+    xf = np.where((pick > 0.99) & (pick < 0.995), xf * np.float32(3e4), xf)
+    x = synth.f32_to_bf16_bits(xf)
+    w = synth.weights(N, K, rng)
+    q, s = oracle.quantize_weight(oracle.E4M3, w)
+    sx = oracle.act_scale(oracle.E4M3, synth.activations(512, K, rng))
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, "e4m3", M, K, N) == "k_fp8_gemm<xq>"
+    xd = to_dev_bf16(x)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = capi.workspace(capi.QLIN_OP_W8A8_LINEAR, "e4m3", M, K, N, device=xd.device)
+    capi.qlin_w8a8_linear("e4m3", xd, to_dev(np.array([sx], np.float32)), to_dev(q), to_dev(s), None, y, ws)
+    torch.cuda.synchronize()
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    got = ws.view(torch.uint8)[: M * K].cpu().numpy().reshape(M, K)
+    ref = oracle.quantize_act(oracle.E4M3, x, sx)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:4].tolist()}"
+    assert (ref == 0x80).any() and (ref == 0xFE).any()  # -0 and -448 both occur

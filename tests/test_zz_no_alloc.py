@@ -70,7 +70,11 @@ def test_noalloc_rejects_sizes_beyond_scratch(capi):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for qt in ("int8", "e4m3"):
         need = lambda M: capi.qlin_workspace_bytes(capi.QLIN_OP_W8A8_LINEAR, qt, M, K, N)
-        m_max = limit // need(1)
+        lo, hi = 1, limit  # need() grows with M: the largest M whose workspace fits
+        while lo < hi:
+            mid = (lo + hi + 1) // 2
+            lo, hi = (mid, hi) if need(mid) <= limit else (lo, mid - 1)
+        m_max = lo
         assert need(m_max) <= limit < need(m_max + 1)
         st = L.qlin_w8a8_linear_noalloc(capi.QTYPES[qt], m_max + 1, K, N, p, p, p, p, None, p, stream)
         assert st == capi.QLIN_ERR_WORKSPACE
