@@ -27,6 +27,7 @@
 // same exit path (TMEM freed, cluster barriers met).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -161,6 +162,15 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (p.K + C::BK - 1) / C::BK;
+  if constexpr (MC == 2) {
+    // Launched without its 2-CTA cluster shape, the pair's multicasts and peer
+    // barrier arrivals would address a CTA that does not exist: report and leave
+    // before any barrier, TMEM or peer is touched.
+    if (cluster_nctarank() != 2) {
+      if (threadIdx.x == 0) set_status(p.status, QLIN_ERR_UNSUPPORTED);
+      return;
+    }
+  }
   // work items: tiles (MC = 1) or tile pairs (MC = 2: m-tiles 2q, 2q+1 of one n-tile)
   const int rank = MC == 2 ? (int)cluster_ctarank() : 0;
   const int mgroups = (p.mtiles + MC - 1) / MC;
@@ -275,6 +285,9 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
           }
         }
       }
+      // abort: the stages this CTA armed land before it leaves (with a pair, a
+      // stage whose peer half never comes gives up after the drain limit)
+      if (*abort_flag) drain_ring(full, C::STAGES, i, C::STAGES);
     }
   } else if (XQ == 1 && (warp == 2 || warp == 3 || warp >= 12)) {  // ----- activation quantizer
     uint64_t *xq_full = (uint64_t *)(smem + C::BAR_OFF + 128), *xq_empty = xq_full + C::XQ_NBUF;
@@ -433,8 +446,9 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         mma_commit(&acc_full[b]);
       }
       // Drain: no commit arrival may still be in flight towards this CTA's shared
-      // memory when it exits (a successor CTA on this SM may already own it).
-      if (i > 0) ok = mbar_wait(&empty[(i - 1) % C::STAGES], ((i - 1) / C::STAGES) & 1, abort_flag) && ok;
+      // memory when it exits (a successor CTA on this SM may already own it); the
+      // wait holds on the abort path too
+      if (i > 0) ok = mbar_wait_drain(&empty[(i - 1) % C::STAGES], ((i - 1) / C::STAGES) & 1) && ok;
       if (!ok) *abort_flag = 1;
     }
   } else if (warp >= 4) {  // ------------------------- epilogue
@@ -530,8 +544,12 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   // neither CTA of a pair leaves while the other may still multicast into it or
-  // arrive on its barriers (every wait above is bounded, so both get here)
-  if constexpr (MC == 2) cluster_sync();
+  // arrive on its barriers (every wait above is bounded, so both get here); on
+  // the abort path what the peer sent before the barrier is given time to land
+  if constexpr (MC == 2) {
+    cluster_sync();
+    if (*abort_flag) peer_grace();
+  }
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -728,6 +746,13 @@ __global__ void __launch_bounds__(640, 1)
   float *xchg = reinterpret_cast<float *>(smem + C::XCHG_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.z, S = p.splits;
+  // The split-K reduction reads the partial tiles of S cluster peers through
+  // distributed shared memory: without that cluster shape, report and leave
+  // before any barrier, TMEM or peer is touched.
+  if (S > 1 && (int)cluster_nctarank() != S) {
+    if (threadIdx.x == 0) set_status(p.status, QLIN_ERR_UNSUPPORTED);
+    return;
+  }
   const int KB = (p.K + C::BK - 1) / C::BK;
   const int kb0 = (int)((int64_t)split * KB / S), kb1 = (int)((int64_t)(split + 1) * KB / S);
   const int nkb = kb1 - kb0;
@@ -791,6 +816,7 @@ __global__ void __launch_bounds__(640, 1)
           }
         }
       }
+      if (*abort_flag) drain_ring(raw_full, C::R, i, C::R);  // abort: armed stages land first
     }
   } else if (warp == 2) {  // ----------------- activation-tile producer
     if (lane == 0) {
@@ -807,6 +833,7 @@ __global__ void __launch_bounds__(640, 1)
           tma_load_2d(&tm_x, &x_full[s], xs + s * C::X_BYTES, (kb0 + kb) * C::BK, m0);
         }
       }
+      if (*abort_flag) drain_ring(x_full, C::X, i, C::X);  // abort: armed stages land first
     }
   } else if (warp == 1 || (warp == 3 && C::ISSUERS == 2)) {  // -- MMA issuers
     // Issuer e (warp 1: e = 0, warp 3: e = 1) takes the k-blocks with kb % ISSUERS == e
@@ -854,10 +881,11 @@ __global__ void __launch_bounds__(640, 1)
         }
       }
       // Drain: the CTA must not exit with a commit arrival still in flight towards
-      // its shared memory (a successor CTA on this SM may already own it).
+      // its shared memory (a successor CTA on this SM may already own it); the
+      // waits hold on the abort path too
       if (last >= 0) {
-        ok = mbar_wait(&x_empty[last % C::X], (last / C::X) & 1, abort_flag) &&
-             mbar_wait(&a_empty[last % C::NA], (last / C::NA) & 1, abort_flag) && ok;
+        ok = mbar_wait_drain(&x_empty[last % C::X], (last / C::X) & 1) &&
+             mbar_wait_drain(&a_empty[last % C::NA], (last / C::NA) & 1) && ok;
       }
       if (!ok) *abort_flag = 1;
     }
@@ -1299,8 +1327,16 @@ size_t fp8_xq_flag_bytes(int64_t M, int64_t K) {
 // large share of the work); on wider GEMMs the separate quantization pass is as
 // fast or faster.  Its quantizers are the GEMM's CTAs, so the tile pairs must
 // fill every SM.  N counts GEMM columns (2I for the merged gate_up).
+// QLIN_FP8_FUSED_QUANT=0 in the environment (read once) keeps the separate
+// quantization pass everywhere: a profiler that re-issues cooperative launches
+// without their cluster shape cannot run the fused kernel.
 bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms) {
   (void)K;
+  static const bool enabled = [] {
+    const char *v = std::getenv("QLIN_FP8_FUSED_QUANT");
+    return !(v && v[0] == '0' && v[1] == 0);
+  }();
+  if (!enabled) return false;
   const int64_t mtiles = (M + Fp8Cfg::BM - 1) / Fp8Cfg::BM, ntiles = (N + Fp8Cfg::BN - 1) / Fp8Cfg::BN;
   return mtiles >= 16 && N <= 4096 && ((mtiles + 1) / 2) * ntiles >= sms / 2;
 }

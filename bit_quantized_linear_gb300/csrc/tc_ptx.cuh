@@ -59,15 +59,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
-// Waits (bounded, whatever the abort flag says) for copies this CTA issued to
-// land before it leaves: no async write may reach shared memory the next CTA
-// on the SM already owns.
+// Waits (bounded, whatever the abort flag says) for copies or MMA commits this
+// CTA issued to land before it leaves: no async write may reach shared memory
+// the next CTA on the SM already owns.  A copy in flight lands within
+// microseconds; the limit only ends waits for phases that can no longer
+// complete (a peer that stopped before sending its half).
+constexpr uint64_t kDrainLimitNs = 20000000ull;  // 20 ms
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
   const uint32_t addr = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(addr, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return false;
   return true;
+}
+// The last `window` phases of a ring whose slot k % stages took use k, for the
+// `issued` uses made (older uses were waited for before their slots were
+// reused), each waited for as above.
+__device__ __forceinline__ void drain_ring(uint64_t *bars, int stages, int issued, int window) {
+  for (int k = issued > window ? issued - window : 0; k < issued; ++k)
+    mbar_wait_drain(&bars[k % stages], (uint32_t)(k / stages) & 1);
+}
+// After a cluster's CTAs have all stopped issuing (past a cluster barrier), the
+// copies and commit arrivals a peer sent towards this CTA before that barrier
+// are given time to land before the CTA leaves (abort path only).
+constexpr uint64_t kPeerGraceNs = 1000000ull;  // 1 ms
+__device__ __forceinline__ void peer_grace() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < kPeerGraceNs) __nanosleep(1000);
 }
 
 // Named barrier `id` over `nthreads` threads (a multiple of 32) that also ANDs
@@ -310,6 +328,12 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// CTAs in this CTA's cluster (1 for a launch without a cluster shape).
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 __device__ __forceinline__ void cluster_sync() {

@@ -36,7 +36,9 @@
  *   - M == 0 is valid and enqueues nothing.
  *   - Device-side waits in the kernels are bounded; a wait that runs out sets
  *     a device status word instead of hanging, which qlin_get_device_status()
- *     reports as QLIN_ERR_TIMEOUT.
+ *     reports as QLIN_ERR_TIMEOUT.  A kernel whose cluster shape is not the
+ *     one it was launched for (a tool that re-issues the launch without it)
+ *     does no work and sets QLIN_ERR_UNSUPPORTED there.
  */
 #ifndef QLIN_H_
 #define QLIN_H_
@@ -54,7 +56,9 @@ typedef struct CUstream_st *qlin_stream_t;
 typedef enum {
   QLIN_OK = 0,
   QLIN_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misalignment, K/N % 16 != 0 */
-  QLIN_ERR_UNSUPPORTED = 2, /* no device, not sm_103, or qtype not valid here */
+  QLIN_ERR_UNSUPPORTED = 2, /* no device, not sm_103, qtype not valid here, or
+                               (device status) a kernel launched without its
+                               cluster shape */
   QLIN_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes < qlin_workspace_bytes() */
   QLIN_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   QLIN_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (device status) */
@@ -157,6 +161,13 @@ qlin_status qlin_w8a16_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N,
  *   qtype, w_scale [N], bias [N] BF16 or NULL, y [M,N] BF16.
  *   ws: qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N) bytes.
  * Requirements as for qlin_w8a16_linear.
+ * Execution: for E4M3 with at least 16 token tiles of 128 and N <= 4096 the
+ * quantization runs inside the GEMM kernel (a cooperative launch of 2-CTA
+ * clusters); the codes still land in the workspace.  QLIN_FP8_FUSED_QUANT=0 in
+ * the environment (read once per process) selects the separate quantization
+ * pass instead, e.g. under a profiler that re-issues cooperative launches
+ * without their cluster shape (the fused kernel would report
+ * QLIN_ERR_UNSUPPORTED there).  Same results either way.
  */
 qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
                              const float *input_scale, const void *qw, const float *w_scale,

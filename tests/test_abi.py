@@ -122,3 +122,23 @@ def test_no_device_is_reported_not_crashed(capi):
     good = P(4096)
     st = L.qlin_w8a16_linear(0, 1, 64, 64, good, good, good, None, good, None, 0, None)
     assert st in (capi.QLIN_ERR_UNSUPPORTED, capi.QLIN_ERR_CUDA)
+
+
+def test_fused_quant_switch_selects_the_separate_pass():
+    """QLIN_FP8_FUSED_QUANT=0 (read once per process) routes E4M3 W8A8 through
+    the separate quantization pass, for every size."""
+    import subprocess
+    import sys
+    code = ("from bit_quantized_linear_gb300 import capi; "
+            "print(capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 2048)); "
+            "print(capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 1024))")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, QLIN_FP8_FUSED_QUANT="0", PYTHONPATH=root)
+    out = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.split() == ["k_quantize_act+k_fp8_gemm"] * 2
+    env["QLIN_FP8_FUSED_QUANT"] = "1"
+    out = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True, text=True,
+                         timeout=300)
+    assert out.stdout.split() == ["k_fp8_gemm<xq>"] * 2
