@@ -335,7 +335,8 @@ def w8a16_gate_up_silu(qtype, x, qw, w_scale, bias=None):
     M, K = x.shape
     I = qw.shape[0] // 2
     y = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
-    qlin_w8a16_gate_up_silu(qtype, x, qw, w_scale, bias, y)
+    ws = workspace(QLIN_OP_W8A16_GATE_UP_SILU, qtype, M, K, I, device=x.device)
+    qlin_w8a16_gate_up_silu(qtype, x, qw, w_scale, bias, y, ws)
     return y
 
 

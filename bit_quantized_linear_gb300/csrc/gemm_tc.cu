@@ -115,12 +115,15 @@ template <int XQ>
 struct Fp8CfgT {
   static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages : 4;
   static constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  // XQ: a ring of chunks (64 rows of a task's 128 x 128 BF16 activation tile),
-  // TMA-staged, as many as the rest of the shared memory holds
-  static constexpr int XQ_CHUNK = (BM / 2) * BK * 2, XQ_OFF = BAR_OFF + 256;
-  static constexpr int XQ_NBUF = XQ ? (227 * 1024 - XQ_OFF - 1024) / XQ_CHUNK : 0;
-  static constexpr int SMEM = XQ_OFF + XQ_NBUF * XQ_CHUNK + 1024;
+  // epilogue: one 32 x 32 BF16 block per epilogue warp, staged for a TMA store
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES, EPI_WARP_BYTES = 32 * 32 * 2, EPI_BYTES = 8 * EPI_WARP_BYTES;
+  // XQ: a ring of chunks (XQ_ROWS rows of a task's 128 x 128 BF16 activation
+  // tile), TMA-staged, as many as the rest of the shared memory holds
+  static constexpr int XQ_ROWS = 32, XQ_CPT = BM / XQ_ROWS, XQ_CHUNK = XQ_ROWS * BK * 2;
+  static constexpr int XQ_OFF = EPI_OFF + EPI_BYTES;
+  static constexpr int XQ_NBUF = XQ ? (227 * 1024 - XQ_OFF - 256 - 1024) / XQ_CHUNK : 0;
+  static constexpr int BAR_OFF = XQ_OFF + XQ_NBUF * XQ_CHUNK;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr int THREADS = XQ ? 512 : 384;
   static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, BN);
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -150,7 +153,7 @@ using Fp8Cfg = Fp8CfgT<0>;
 template <int MC, int XQ>
 __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-               const __grid_constant__ CUtensorMap tm_x, Fp8Params p) {
+               const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, Fp8Params p) {
   using C = Fp8CfgT<XQ>;
   static_assert(MC == 1 || MC == 2, "cluster of one or two CTAs");
   extern __shared__ uint8_t smem_raw[];
@@ -192,6 +195,7 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_y);
     if constexpr (XQ == 1) {
       uint64_t *xq_full = (uint64_t *)(smem + C::BAR_OFF + 128), *xq_empty = xq_full + C::XQ_NBUF;
       unsigned *xq_count = (unsigned *)(xq_empty + C::XQ_NBUF);
@@ -301,9 +305,9 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
       kb = r / nb;
       mt = band * p.xq_band + (r - kb * nb);
     };
-    // chunk c = half c & 1 of task c >> 1 goes through ring buffer c % NB
-    constexpr int NB = C::XQ_NBUF;
-    const int chunks = 2 * mine;
+    // chunk c = part c % CPT (XQ_ROWS rows) of task c / CPT goes through ring buffer c % NB
+    constexpr int NB = C::XQ_NBUF, CPT = C::XQ_CPT;
+    const int chunks = CPT * mine;
     if (warp == 2) {  // ---- staging: TMA loads of BF16 chunks into the ring
       if (lane == 0) {
         // chunks kXqPrefetch ahead of the one being loaded are brought into L2,
@@ -311,8 +315,8 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         auto prefetch = [&](int c) {
           if (c >= chunks) return;
           int mt, kb;
-          task_of(c >> 1, mt, kb);
-          tma_prefetch_l2_2d(&tm_x, kb * C::BK, mt * C::BM + (c & 1) * (C::BM / 2));
+          task_of(c / CPT, mt, kb);
+          tma_prefetch_l2_2d(&tm_x, kb * C::BK, mt * C::BM + (c % CPT) * C::XQ_ROWS);
         };
         for (int c = 0; c < kXqPrefetch; ++c) prefetch(c);
         // the BF16 activations are read once: they must not push the GEMM's
@@ -328,10 +332,10 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
             break;
           }
           int mt, kb;
-          task_of(c >> 1, mt, kb);
+          task_of(c / CPT, mt, kb);
           mbar_arrive_expect_tx(&xq_full[b], C::XQ_CHUNK);
           tma_load_2d_hint(&tm_x, &xq_full[b], (void *)(xq_buf + b * C::XQ_CHUNK), kb * C::BK,
-                           mt * C::BM + (c & 1) * (C::BM / 2), policy);
+                           mt * C::BM + (c % CPT) * C::XQ_ROWS, policy);
         }
         if (!ok) {
           *abort_flag = 1;
@@ -380,14 +384,14 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
           break;
         }
         int mt, kb;
-        task_of(c >> 1, mt, kb);
+        task_of(c / CPT, mt, kb);
         const uint32_t src = smem_u32(xq_buf + b * C::XQ_CHUNK);
-        const int mh = mt * C::BM + (c & 1) * (C::BM / 2), k0 = kb * C::BK;
-        // 64 rows x 16 pieces of 8 BF16 (16 consecutive threads cover one row's
-        // 256 bytes): each thread reads its eight pieces first, then converts
-        // and stores them, eight independent chains
-        constexpr int PIECES = (C::BM / 2) * 16 / (32 * kXqConverters);
-        static_assert(PIECES * 32 * kXqConverters == (C::BM / 2) * 16, "pieces per converter thread");
+        const int mh = mt * C::BM + (c % CPT) * C::XQ_ROWS, k0 = kb * C::BK;
+        // XQ_ROWS rows x 16 pieces of 8 BF16 (16 consecutive threads cover one
+        // row's 256 bytes): each thread reads its pieces first, then converts and
+        // stores them, independent chains
+        constexpr int PIECES = C::XQ_ROWS * 16 / (32 * kXqConverters);
+        static_assert(PIECES * 32 * kXqConverters == C::XQ_ROWS * 16, "pieces per converter thread");
         uint4 v[PIECES];
 #pragma unroll
         for (int i = 0; i < PIECES; ++i) v[i] = lds128(src + 16u * (qt + i * 32 * kXqConverters));
@@ -410,7 +414,7 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         __syncwarp();  // the warp's reads of the buffer and its code stores come before ...
         if (lane == 0) {
           mbar_arrive(&xq_empty[b]);                                             // ... the refill
-          if (c & 1) red_release_cta_shared_add(&xq_count[warp - 12], 1u);     // ... the publication
+          if (c % CPT == CPT - 1) red_release_cta_shared_add(&xq_count[warp - 12], 1u);  // ... the publication
         }
       }
     }
@@ -455,6 +459,54 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     const int q4 = warp & 3, half = (warp - 4) >> 2;  // half h owns channels [128h, 128h + 128)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float sx = p.xs_per_token ? 1.0f : __ldg(p.x_scale);
+    // Output path: each 32 x 32 block of BF16 results (row = lane) is written into
+    // this warp's staging block with the 64-byte swizzle (16-byte chunk q of row r
+    // at chunk q ^ ((r >> 1) & 3): the lanes' row writes hit distinct banks), then
+    // stored by TMA, which writes whole row segments and clips rows and columns
+    // outside y.
+    uint8_t *stage = smem + C::EPI_OFF + (warp - 4) * C::EPI_WARP_BYTES;
+    const uint32_t st_row = smem_u32(stage) + 64u * lane, sw = (lane >> 1) & 3;
+    bool pending = false;  // lane 0 has a store in flight that reads the staging block
+    auto emit = [&](const uint32_t (&o)[16], int x, int y) {
+      if (pending) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        sts128(st_row + (((uint32_t)q ^ sw) << 4), make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+      fence_proxy_async_smem();  // the TMA store reads the block through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tm_y, stage, x, y);
+        bulk_commit();
+      }
+      pending = true;
+    };
+    // Column factors of 8 channels from n (the same for every lane: broadcast
+    // loads): scale s_x * s_w[n + i] and bias; zero from channel `end` on (n is a
+    // multiple of 8 and end of 16, so the 8 are all inside or all outside).  end
+    // is N, or 2N for the up channels of the merged gate_up weight.
+    auto col_factors = [&](int n, int end, float (&sc)[8], float (&bi)[8]) {
+      if (n < end) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(p.w_scale + n);
+        const float4 v0 = __ldg(w4), v1 = __ldg(w4 + 1);
+        sc[0] = sx * v0.x, sc[1] = sx * v0.y, sc[2] = sx * v0.z, sc[3] = sx * v0.w;
+        sc[4] = sx * v1.x, sc[5] = sx * v1.y, sc[6] = sx * v1.z, sc[7] = sx * v1.w;
+        if (p.bias) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.bias + n));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) bi[2 * e] = bf16_bits_to_f32(w[e] & 0xFFFFu), bi[2 * e + 1] = bf16_bits_to_f32(w[e] >> 16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bi[i] = 0.0f;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[i] = 0.0f, bi[i] = 0.0f;
+      }
+    };
     bool ok = true;
     for (int j = 0; j < my_tiles && ok; ++j) {
       const int t = cid + j * G, b = j & 1;
@@ -466,8 +518,7 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         ok = false;
         break;
       }
-      const int m = m0 + q4 * 32 + lane;
-      uint16_t *yrow = p.y + (size_t)m * p.N;
+      const int m = m0 + q4 * 32 + lane, yrow0 = m0 + q4 * 32;
       // per-token activation scale multiplies the row (lane = token)
       const float sxm = p.xs_per_token ? (m < p.M ? __ldg(p.x_scale + m) : 0.0f) : 1.0f;
       if (p.glu) {
@@ -476,67 +527,65 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         const int nb0 = n0 / 2;
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
-          uint32_t rg[32], ru[32];
-          tmem_ld32(tmem + lane_base + b * C::BN + c, rg);
-          tmem_ld32(tmem + lane_base + b * C::BN + 128 + c, ru);
           const int nb = nb0 + c;
-          const float sg = sx * __ldg(p.w_scale + nb + lane), su = sx * __ldg(p.w_scale + p.N + nb + lane);
-          const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + nb + lane)) : 0.0f;
-          const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + nb + lane)) : 0.0f;
-          tmem_ld_wait();
           uint32_t o[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            float v[2];
+          for (int q = 0; q < 2; ++q) {  // 16 gate columns and their 16 up columns at a time
+            uint32_t rg[16], ru[16];
+            tmem_ld16(tmem + lane_base + b * C::BN + c + 16 * q, rg);
+            tmem_ld16(tmem + lane_base + b * C::BN + 128 + c + 16 * q, ru);
+            tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = 2 * h + e;
-              const float g = fmaf(__uint_as_float(rg[col]), sxm * __shfl_sync(0xffffffffu, sg, col),
-                                   __shfl_sync(0xffffffffu, bg, col));
-              const float u = fmaf(__uint_as_float(ru[col]), sxm * __shfl_sync(0xffffffffu, su, col),
-                                   __shfl_sync(0xffffffffu, bu, col));
-              v[e] = silu_f(g) * u;
+            for (int hh = 0; hh < 2; ++hh) {
+              // gate channels nb + 16q + 8hh.., and the up channels N further on (N % 16 == 0)
+              float sg[8], bg[8], su[8], bu[8];
+              col_factors(nb + 16 * q + 8 * hh, p.N, sg, bg);
+              col_factors(p.N + nb + 16 * q + 8 * hh, 2 * p.N, su, bu);
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                float v[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int i = 2 * h + e, col = 8 * hh + i;
+                  const float g = fmaf(__uint_as_float(rg[col]), sxm * sg[i], bg[i]);
+                  const float u = fmaf(__uint_as_float(ru[col]), sxm * su[i], bu[i]);
+                  v[e] = silu_f(g) * u;
+                }
+                o[8 * q + 4 * hh + h] = pack_bf16x2(v[0], v[1]);
+              }
             }
-            o[h] = pack_bf16x2(v[0], v[1]);
           }
-          if (m < p.M) {
-            uint4 *dst = reinterpret_cast<uint4 *>(yrow + nb);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
-          }
+          emit(o, nb, yrow0);
         }
       } else {
 #pragma unroll 1
-      for (int c = 128 * half; c < 128 * half + 128; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + b * C::BN + c, r);
-        const int nb = n0 + c;
-        // column factors of this 32-column group: lane l holds column nb + l, shuffled below
-        const bool cv = nb + lane < p.N;
-        const float scl = cv ? sx * __ldg(p.w_scale + nb + lane) : 0.0f;
-        const float bia = (cv && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + nb + lane)) : 0.0f;
-        tmem_ld_wait();
-        uint32_t o[16];
+        for (int c = 128 * half; c < 128 * half + 128; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + b * C::BN + c, r);
+          const int nb = n0 + c;
+          tmem_ld_wait();
+          uint32_t o[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float v0 = fmaf(__uint_as_float(r[2 * h]), sxm * __shfl_sync(0xffffffffu, scl, 2 * h),
-                                __shfl_sync(0xffffffffu, bia, 2 * h));
-          const float v1 = fmaf(__uint_as_float(r[2 * h + 1]), sxm * __shfl_sync(0xffffffffu, scl, 2 * h + 1),
-                                __shfl_sync(0xffffffffu, bia, 2 * h + 1));
-          o[h] = pack_bf16x2(v0, v1);
-        }
-        if (m < p.M && nb < p.N) {
-          uint4 *dst = reinterpret_cast<uint4 *>(yrow + nb);
+          for (int hh = 0; hh < 4; ++hh) {
+            float sc[8], bi[8];
+            col_factors(nb + 8 * hh, p.N, sc, bi);
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (nb + 8 * g < p.N) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+            for (int h = 0; h < 4; ++h) {
+              const int i = 2 * h, col = 8 * hh + i;
+              o[4 * hh + h] = pack_bf16x2(fmaf(__uint_as_float(r[col]), sxm * sc[i], bi[i]),
+                                          fmaf(__uint_as_float(r[col + 1]), sxm * sc[i + 1], bi[i + 1]));
+            }
+          }
+          if (nb < p.N) emit(o, nb, yrow0);
         }
-      }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
+    // every store has written y (and read its staging block) before the CTA leaves
+    if (lane == 0 && pending) bulk_wait_all();
+    __syncwarp();
     if (!ok) *abort_flag = 1;
   }
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, QLIN_ERR_TIMEOUT);
@@ -1244,13 +1293,15 @@ static cudaError_t set_smem(KernelT kernel, int bytes) {
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st) {
   if (g.M == 0) return cudaSuccess;
   using C = Fp8Cfg;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, ty;
   // glu: the weight has 2N rows and a tile takes 128 gate rows plus their 128 up rows (two boxes)
   const int64_t wrows = g.glu ? 2 * g.N : g.N;
-  // B is loaded as two boxes of 128 rows (two halves of the 256-row tile)
+  // B is loaded as two boxes of 128 rows (two halves of the 256-row tile); y [M, N]
+  // (N = I for glu) is written in 32 x 32 blocks through a 64-byte-swizzled staging block
   if (!make_map(&ta, g.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.M, g.K, C::BK, C::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&tb, g.qw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wrows, g.K, C::BK, C::BN / 2,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&ty, g.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   // glu: an output tile is 128 channels (n0 counts the 256 gate+up columns of the MMA tile)
   const int mtiles = (int)((g.M + C::BM - 1) / C::BM);
@@ -1266,8 +1317,8 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   };
   if (g.xq) {  // fused quantization: cooperative launch; pairs share B where clusters combine with it
     if (g.x_scale_per_token || !g.xq_flags) return cudaErrorInvalidValue;
-    CUtensorMap tx;  // the BF16 activations, chunks of 64 rows of a 128 x 128 task tile
-    if (!make_map(&tx, g.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, C::BM / 2,
+    CUtensorMap tx;  // the BF16 activations, chunks of XQ_ROWS rows of a 128 x 128 task tile
+    if (!make_map(&tx, g.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, Fp8CfgT<1>::XQ_ROWS,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const size_t fb = fp8_xq_flag_bytes(g.M, g.K);
@@ -1282,7 +1333,7 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
       const int grid = 2 * (items < pairs ? items : pairs);
       p.xq_band = band(grid / 2, 2);
       e = launch_kernel_coop(k_fp8_gemm<2, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 2, ta, tb,
-                             tx, p);
+                             tx, ty, p);
       if (e == cudaSuccess) return e;
       pairs_ok = false;
     }
@@ -1290,19 +1341,19 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
     const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
     p.xq_band = band(grid, 1);
     return launch_kernel_coop(k_fp8_gemm<1, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 1, ta, tb,
-                              tx, p);
+                              tx, ty, p);
   }
   if (mtiles >= 2) {  // pairs of m-tiles share their B tiles (2-CTA clusters, TMA multicast)
     static cudaError_t attr2 = set_smem(k_fp8_gemm<2, 0>, C::SMEM);
     if (attr2 != cudaSuccess) return attr2;
     const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
     const int grid = 2 * (items < pairs ? items : pairs);
-    return launch_kernel_x(k_fp8_gemm<2, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 2, ta, tb, tb, p);
+    return launch_kernel_x(k_fp8_gemm<2, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 2, ta, tb, tb, ty, p);
   }
   static cudaError_t attr = set_smem(k_fp8_gemm<1, 0>, C::SMEM);
   if (attr != cudaSuccess) return attr;
   const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-  return launch_kernel(k_fp8_gemm<1, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, p);
+  return launch_kernel(k_fp8_gemm<1, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, ty, p);
 }
 
 // Token tile (MMA N) of the W8A16 swap-AB kernel.  Up to 128 tokens the tile

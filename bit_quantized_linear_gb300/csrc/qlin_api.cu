@@ -104,6 +104,13 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_W8A16_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
+      if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) {
+        return w8a16_f8_tt(M) == 16 ? "k_w8a16_split+k_w8a16_f8<16>" : "k_w8a16_split+k_w8a16_f8<32>";
+      }
+      if (M <= kW8GemvMaxM) {
+        static const char *gv[4] = {"k_w8_gemv<1>", "k_w8_gemv<2>", "k_w8_gemv<4>", "k_w8_gemv<8>"};
+        return gv[M <= 1 ? 0 : M <= 2 ? 1 : M <= 4 ? 2 : 3];
+      }
       static const char *names[5] = {"k_w8_dq<16>", "k_w8_dq<32>", "k_w8_dq<64>", "k_w8_dq<128>", "k_w8_dq<256>"};
       const int b = w8_swap_bnt(M, N, K, sm_count());
       return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : b == 128 ? 3 : 4];
@@ -170,7 +177,10 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     case QLIN_OP_QUANTIZE_WEIGHT: return 0;
     case QLIN_OP_ACT_SCALE: return 256;
     case QLIN_OP_QUANTIZE_ACT: return 0;
-    case QLIN_OP_W8A16_LINEAR: return 0;
+    // E4M3 up to kW8A16F8MaxM tokens: the activations' two E4M3 terms and per-token scales
+    case QLIN_OP_W8A16_LINEAR:
+    case QLIN_OP_W8A16_GATE_UP_SILU:
+      return (qtype == QLIN_E4M3 && M > 0 && M <= kW8A16F8MaxM) ? w8a16_f8_workspace(M, K) : 0;
     // quantized activations: E4M3 codes (1 byte) and, for the fused-quantization GEMM, its
     // task flags; or INT8 codes as integer-valued BF16 (2 bytes)
     case QLIN_OP_W8A8_LINEAR:
@@ -183,7 +193,6 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
       return round_up((size_t)M * (size_t)K * (qtype == QLIN_INT8 ? 2 : 1), 256) + round_up((size_t)M * 4, 256);
     case QLIN_OP_KV_STORE_MIXED:
     case QLIN_OP_KV_LOAD_MIXED:
-    case QLIN_OP_W8A16_GATE_UP_SILU:
       return 0;
   }
   return (size_t)-1;
@@ -238,6 +247,10 @@ qlin_status qlin_w8a16_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N,
   if (qlin_status s = current_device(&dev)) return s;
   if (M == 0) return QLIN_OK;
   GemmArgs g{kW8A16, qtype, M, K, N, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
+  // E4M3 weights, small batch: FP8 MMAs on the codes against the split activations
+  if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) return from_cuda(launch_w8a16_f8(g, ws, *dev, (cudaStream_t)stream));
+  // INT8 weights, a handful of tokens: a weight-streaming matrix-vector product on the CUDA cores
+  if (M <= kW8GemvMaxM) return from_cuda(launch_w8_gemv(g, *dev, (cudaStream_t)stream));
   return from_cuda(launch_w8a16_swap(g, *dev, (cudaStream_t)stream));
 }
 
@@ -329,13 +342,15 @@ qlin_status qlin_w8a16_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int6
   if (qlin_status s = check_glu_shape(M, K, I)) return s;
   if (!qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias))) return QLIN_ERR_INVALID_ARG;
   if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
-  (void)ws;
-  (void)ws_bytes;
+  const size_t need = qlin_workspace_bytes(QLIN_OP_W8A16_GATE_UP_SILU, qtype, M, K, I);
+  if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
   DeviceInfo *dev;
   if (qlin_status s = current_device(&dev)) return s;
   if (M == 0) return QLIN_OK;
   GemmArgs g{kW8A16, qtype, M, K, I, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
   g.glu = 1;
+  if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) return from_cuda(launch_w8a16_f8(g, ws, *dev, (cudaStream_t)stream));
+  if (M <= kW8GemvMaxM) return from_cuda(launch_w8_gemv(g, *dev, (cudaStream_t)stream));
   return from_cuda(launch_w8a16_swap(g, *dev, (cudaStream_t)stream));
 }
 

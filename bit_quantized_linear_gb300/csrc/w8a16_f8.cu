@@ -1,0 +1,407 @@
+// W8A16 linear (BF16 activations, 8-bit weight codes with per-channel scales)
+// on the FP8 tensor cores, with no per-code conversion of the weights
+// ("Nano-vLLM-MoE" README, "FP8 W8A16 weight-only quantization": FP8 weights
+// dequantized to BF16 for a BF16 x BF16 product with fp32 accumulation).
+//
+// The weight stream is the cost of a small-batch linear, and turning every code
+// into BF16 before a BF16 MMA costs more issue slots than the stream leaves.
+// Instead the activations, which are few, are put into the weights' format:
+// each token row x_m gets a power-of-two scale s_m (the least with
+// 448 s_m >= max |x_m|), and x_m / s_m is split into two E4M3 terms
+//     x1 = RN_e4m3(x / s),  x2 = RN_e4m3(16 (x / s - x1)),  x / s = x1 + x2 / 16.
+// For |x / s| >= 2^-6 the split is exact: x1 keeps the leading 4 significant
+// bits, the remainder is a multiple of 2^(e-7) below 2^(e-3) (e the exponent of
+// x / s), so 16 times it has at most 4 significant bits from 2^(e-3) >= 2^-9
+// upwards, which E4M3 holds.  Smaller elements (|x| below about 2^-13.8 of the
+// row's maximum) are kept to an absolute error of 2^-14 s.  Then
+//     sum_k w[n,k] x[m,k] = s_m (sum_k w x1 + (1/16) sum_k w x2),
+// two FP8 products read straight from the weight codes: one E4M3 MMA with the
+// two terms of every token as 2 x BNT columns of the B operand (swap AB: the
+// weight rows are the MMA's 128 rows, so one token still fills the tensor
+// core's M), and an epilogue that forms s_m s_w[n] (acc1 + acc2 / 16) + b[n].
+// INT8 weights: the same with the INT8 codes read as E4M3 would be wrong, so
+// this path is E4M3 only.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace qlin {
+using namespace tc;
+namespace {
+
+// ------------------------------------------------------------ activation split
+// One CTA per token row: the row's abs-max, its power-of-two scale, and the two
+// E4M3 terms written into the B-operand layout: token tile j (tt tokens) owns
+// rows [2 tt j, 2 tt j + 2 tt) of xs, x1 of its tokens first, then x2.
+constexpr int kSplitThreads = 256;
+
+// Least power of two s with 448 s >= a (a > 0), from the exponent bits alone:
+// a = f 2^e with f in [1, 2); 448 = 1.75 2^8, so s = 2^(e-8) when f <= 1.75,
+// else 2^(e-7).  At least 2^-126, so that 1/s is finite (a row that small still
+// fits: 448 2^-126 exceeds every value below 2^-117).
+__device__ __forceinline__ float split_scale(float a) {
+  if (!(a > 0.0f)) return 1.0f;
+  int e;
+  const float f = 2.0f * frexpf(a, &e);  // a = f 2^(e-1), f in [1, 2)
+  return ldexpf(1.0f, max(-126, (e - 1) - (f <= 1.75f ? 8 : 7)));
+}
+
+__global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *__restrict__ x, int M, int K,
+                                                               int tt, uint8_t *__restrict__ xs,
+                                                               float *__restrict__ xscale) {
+  __shared__ float wmax[kSplitThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int m = blockIdx.x;
+  const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
+  const int n8 = K / 8;  // K % 16 == 0
+  float a = 0.0f;
+  for (int i = threadIdx.x; i < n8; i += kSplitThreads) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      a = fmaxf(a, fmaxf(fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)), fabsf(bf16_bits_to_f32(w[e] >> 16))));
+  }
+  a = warp_max(a);
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = a;
+  __syncthreads();
+  a = wmax[0];
+#pragma unroll
+  for (int w = 1; w < kSplitThreads / 32; ++w) a = fmaxf(a, wmax[w]);
+  const float s = split_scale(a), r = 1.0f / s;  // powers of two: exact
+  if (threadIdx.x == 0) xscale[m] = s;
+  const int j = m / tt, t = m % tt;
+  uint8_t *x1 = xs + ((size_t)2 * tt * j + t) * K, *x2 = x1 + (size_t)tt * K;
+  for (int i = threadIdx.x; i < n8; i += kSplitThreads) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4], l[4];  // codes of x1 and x2, two per 16 bits
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float v0 = bf16_bits_to_f32(w[e] & 0xFFFFu) * r, v1 = bf16_bits_to_f32(w[e] >> 16) * r;
+      const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw b1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+      const float2 f1 = __half22float2(__half2(b1));
+      // the remainders are exact in fp32; times 16 they fit E4M3 (see above)
+      const __nv_fp8x2_storage_t c2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v0 - f1.x), 16.0f * (v1 - f1.y)), __NV_SATFINITE, __NV_E4M3);
+      h[e] = c1;
+      l[e] = c2;
+    }
+    *reinterpret_cast<uint2 *>(x1 + 8 * i) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    *reinterpret_cast<uint2 *>(x2 + 8 * i) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+  }
+}
+
+
+// ------------------------------------------------------------ the FP8 linear
+// One CTA per (weight tile, token tile, K split).  Warps: 0 = TMA producer,
+// 1 = TMEM allocator and MMA issuer, 2..5 = epilogue (TMEM lane quadrants
+// 2, 3, 0, 1).  A weight tile is 128 rows (plain) or 64 gate rows and their 64
+// up rows (merged gate_up).  The K splits of a tile form a cluster: each CTA
+// leaves its fp32 partial tile in shared memory (the drained ring) and the
+// cluster sums them in rank order through distributed shared memory, each CTA
+// finishing a slice of the outputs.
+template <int TT>  // token tile; the MMA's N is 2 TT (both terms of each token)
+struct W8F8Cfg {
+  static constexpr int BM = 128, BK = 128, NB = 2 * TT;
+  static constexpr int A_BYTES = BM * BK, B_BYTES = NB * BK, STAGE = A_BYTES + B_BYTES;
+  // about 100 KB of ring, so that two CTAs share an SM and keep the stream busy
+  static constexpr int STAGES = (100 * 1024) / STAGE < 3 ? 3 : (100 * 1024) / STAGE;
+  static constexpr int RING = STAGES * STAGE;
+  static constexpr int PART_BYTES = TT * BM * 4;  // [TT tokens][BM rows] fp32
+  static constexpr int BAR_OFF = RING;
+  static constexpr int SMEM = BAR_OFF + 128 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_COLS = NB;  // 32..256, a power of two
+  static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, NB);
+  static_assert(PART_BYTES <= RING, "partial tile in the ring");
+  static_assert((2 * STAGES + 1) * 8 + 8 <= 128, "barriers");
+  static_assert(STAGE % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
+};
+
+struct W8F8Params {
+  int M, N, K;  // N: output channels (I for the merged gate_up)
+  int glu;
+  int ntiles, splits;
+  const float *w_scale;
+  const float *x_scale;  // per token, from the split
+  const uint16_t *bias;
+  uint16_t *y;
+  unsigned *status;
+};
+
+__device__ __forceinline__ uint8_t *align1k(uint8_t *p) {
+  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int TT>
+__global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
+    k_w8a16_f8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, W8F8Params p) {
+  using C = W8F8Cfg<TT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1k(smem_raw);
+  uint64_t *full = (uint64_t *)(smem + C::BAR_OFF), *empty = full + C::STAGES, *acc_full = empty + C::STAGES;
+  uint32_t *tmem_slot = (uint32_t *)(acc_full + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.splits;
+  // the K splits of a tile reduce through their cluster's shared memory: without
+  // that cluster shape, report and leave before any barrier, TMEM or peer is touched
+  if (S > 1 && (int)cluster_nctarank() != S) {
+    if (threadIdx.x == 0) set_status(p.status, QLIN_ERR_UNSUPPORTED);
+    return;
+  }
+  const int split = blockIdx.z, tile = blockIdx.x % p.ntiles, tj = blockIdx.x / p.ntiles;
+  const int KB = (p.K + C::BK - 1) / C::BK, kb0 = split * KB / S, kb1 = (split + 1) * KB / S, nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0) {  // ------------------------------- TMA producer
+    if (lane == 0) {
+      auto load_w = [&](int i) {
+        uint8_t *st = smem + (i % C::STAGES) * C::STAGE;
+        const int k = (kb0 + i) * C::BK;
+        if (p.glu) {  // 64 gate rows, then their 64 up rows
+          tma_load_2d(&tm_w, &full[i % C::STAGES], st, k, tile * 64);
+          tma_load_2d(&tm_w, &full[i % C::STAGES], st + 64 * C::BK, k, p.N + tile * 64);
+        } else {
+          tma_load_2d(&tm_w, &full[i % C::STAGES], st, k, tile * C::BM);
+        }
+      };
+      auto load_x = [&](int i) {
+        tma_load_2d(&tm_x, &full[i % C::STAGES], smem + (i % C::STAGES) * C::STAGE + C::A_BYTES,
+                    (kb0 + i) * C::BK, tj * C::NB);
+      };
+      // the weights do not depend on the previous kernel of the stream: the first
+      // stages' weight tiles are in flight before its split activations are
+      const int pre = nkb < C::STAGES ? nkb : C::STAGES;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], C::STAGE);
+        load_w(i);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) load_x(i);
+      int i = pre;
+      for (; i < nkb; ++i) {
+        const int s = i % C::STAGES;
+        if (!mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        load_w(i);
+        load_x(i);
+      }
+      if (*abort_flag) drain_ring(full, C::STAGES, i, C::STAGES);  // armed stages land before the CTA leaves
+    }
+  } else if (warp == 1) {  // ------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int i = 0;
+      for (; i < nkb; ++i) {
+        const int s = i % C::STAGES;
+        if (!mbar_wait(&full[s], (i / C::STAGES) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + s * C::STAGE);
+        const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(a + C::A_BYTES);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)  // K = 32 codes per instruction
+          mma_fp8(tmem, ad + 2 * j, bd + 2 * j, C::IDESC, (i > 0 || j > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+      }
+      if (ok) mma_commit(acc_full);
+      // no commit arrival may land after the CTA has left (bounded, also on abort)
+      if (i > 0) ok = mbar_wait_drain(&empty[(i - 1) % C::STAGES], ((i - 1) / C::STAGES) & 1) && ok;
+      if (!ok) *abort_flag = 1;
+    }
+  } else {  // ------------------------------------- epilogue: accumulators -> partial tile
+    const int q4 = warp & 3, r = q4 * 32 + lane;  // TMEM lane = weight row of the tile
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    bool ok = mbar_wait(acc_full, 0, abort_flag);
+    tc_fence_after();
+    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {  // tcgen05.ld is warp-collective
+      float *part = reinterpret_cast<float *>(smem);   // the ring is drained: every MMA has read it
+#pragma unroll 1
+      for (int c = 0; c < TT; c += 16) {
+        uint32_t a1[16], a2[16];  // x1 and x2 products of tokens c..c+15
+        tmem_ld16(tmem + lane_base + c, a1);
+        tmem_ld16(tmem + lane_base + TT + c, a2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          part[(c + t) * C::BM + r] = fmaf(__uint_as_float(a2[t]), 0.0625f, __uint_as_float(a1[t]));
+      }
+    } else {
+      ok = false;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (S > 1) cluster_sync();  // every partial tile of the cluster is written
+
+  // ------------------------------------------- sum over the splits, finish the outputs
+  // this CTA finishes elements [e0, e1) of the tile; consecutive threads take
+  // consecutive rows (channels) of one token, so the stores are coalesced
+  pdl_wait();  // x_scale and y belong to the previous kernels from here on
+  {
+    const int rows = p.glu ? 64 : C::BM, E = TT * rows;
+    const int e0 = split * E / S, e1 = (split + 1) * E / S;
+    const uint32_t pbase = smem_u32(smem);
+    for (int e = e0 + (int)threadIdx.x; e < e1; e += C::THREADS) {
+      const int t = e / rows, rr = e % rows, m = tj * TT + t;
+      if (m >= p.M) continue;
+      auto sum_at = [&](int row) {
+        const uint32_t a = pbase + 4u * (uint32_t)(t * C::BM + row);
+        if (S == 1) return *reinterpret_cast<const float *>(smem + 4 * (t * C::BM + row));
+        float v = 0.0f;
+        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(map_peer_smem(a, (uint32_t)q));  // fixed order
+        return v;
+      };
+      const float sx = __ldg(p.x_scale + m);
+      if (p.glu) {
+        const int n = tile * 64 + rr;
+        const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
+        const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + n)) : 0.0f;
+        const float g = fmaf(sum_at(rr), sx * __ldg(p.w_scale + n), bg);
+        const float u = fmaf(sum_at(64 + rr), sx * __ldg(p.w_scale + p.N + n), bu);
+        p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(silu_f(g) * u);
+      } else {
+        const int n = tile * C::BM + rr;
+        if (n >= p.N) continue;
+        const float b = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
+        p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(fmaf(sum_at(rr), sx * __ldg(p.w_scale + n), b));
+      }
+    }
+  }
+  if (threadIdx.x == 0 && *abort_flag) set_status(p.status, QLIN_ERR_TIMEOUT);
+  __syncthreads();
+  if (S > 1) cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *q = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+            cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)q;
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] bytes, box = 128 columns x box_rows, 128-byte swizzle.
+bool map_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int TT>
+cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const DeviceInfo &dev, cudaStream_t st) {
+  using C = W8F8Cfg<TT>;
+  const int ttiles = (int)((g.M + TT - 1) / TT);
+  CUtensorMap tw, tx;
+  if (!map_u8(&tw, g.qw, g.glu ? 2 * g.N : g.N, g.K, g.glu ? 64 : 128) ||
+      !map_u8(&tx, xs, (int64_t)ttiles * C::NB, g.K, C::NB))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_kernel(k_w8a16_split, dim3((unsigned)g.M), dim3(kSplitThreads), 0, st, 1,
+                                (const uint16_t *)g.a, (int)g.M, (int)g.K, TT, xs, xscale);
+  if (e != cudaSuccess) return e;
+  W8F8Params p;
+  p.M = (int)g.M;
+  p.N = (int)g.N;
+  p.K = (int)g.K;
+  p.glu = g.glu;
+  p.ntiles = g.glu ? (int)(g.N / 64) : (int)((g.N + C::BM - 1) / C::BM);
+  const int units = p.ntiles * ttiles, KB = (int)((g.K + C::BK - 1) / C::BK);
+  p.splits = w8a16_f8_splits(units, KB, dev.sms);
+  p.w_scale = g.w_scale;
+  p.x_scale = xscale;
+  p.bias = g.bias;
+  p.y = (uint16_t *)g.y;
+  p.status = dev.status;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_w8a16_f8<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (attr != cudaSuccess) return attr;
+  return launch_kernel(k_w8a16_f8<TT>, dim3((unsigned)units, 1, (unsigned)p.splits), dim3(C::THREADS), C::SMEM,
+                       st, (unsigned)p.splits, tw, tx, p);
+}
+
+}  // namespace
+
+// Token tile.  Up to kW8A16F8MaxM = 32 tokens: beyond that the two E4M3 terms
+// of the tile (2 tt x 128 bytes a k-block) outweigh the weight tile they meet,
+// and the BF16 path with converted weights is faster.
+int w8a16_f8_tt(int64_t M) { return M <= 16 ? 16 : 32; }
+
+// K splits (a cluster of at most 8 CTAs): the fewest that put a CTA on every
+// SM, keeping at least 4 k-blocks of 128 per CTA.
+int w8a16_f8_splits(int units, int kblocks, int sms) {
+  int s = 1;
+  while (s < 8 && units * s < sms && kblocks / (s + 1) >= 4) ++s;
+  return s;
+}
+
+size_t w8a16_f8_workspace(int64_t M, int64_t K) {
+  const int64_t tt = w8a16_f8_tt(M), ttiles = (M + tt - 1) / tt;
+  return (size_t)((ttiles * 2 * tt * K + 255) / 256 * 256) + (size_t)((M * 4 + 255) / 256 * 256);
+}
+
+cudaError_t launch_w8a16_f8(const GemmArgs &g, void *ws, const DeviceInfo &dev, cudaStream_t st) {
+  if (g.M == 0) return cudaSuccess;
+  if (g.qtype != QLIN_E4M3 || g.M > kW8A16F8MaxM) return cudaErrorInvalidValue;
+  const int64_t tt = w8a16_f8_tt(g.M), ttiles = (g.M + tt - 1) / tt;
+  uint8_t *xs = (uint8_t *)ws;
+  float *xscale = (float *)((uint8_t *)ws + (ttiles * 2 * tt * g.K + 255) / 256 * 256);
+  return tt == 16 ? launch_tt<16>(g, xs, xscale, dev, st) : launch_tt<32>(g, xs, xscale, dev, st);
+}
+
+}  // namespace qlin

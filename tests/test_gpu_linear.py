@@ -71,6 +71,43 @@ def test_w8a16_ragged_kn(capi, qt, M, K, N):
     w8a16_case(capi, qt, M, K, N, M % 2 == 1, "ragged-kn", outliers=True)
 
 
+@pytest.mark.parametrize("M,K,N", [(4, 1040, 1040), (6, 528, 2064), (7, 18944, 64), (2, 3584, 9472), (8, 16, 4096),
+                                   (1, 2064, 32), (3, 3600, 4112)])
+def test_w8a16_int8_cuda_core_path_edges(capi, M, K, N):
+    """Up to 8 tokens INT8 W8A16 runs as a matrix-vector product on the CUDA
+    cores: token counts below the kernel's template width, K not a multiple of
+    its 512-code step (and K = 16), and few output rows, where K is split over 2
+    or 4 warps whose partial sums meet in shared memory."""
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, "int8", M, K, N).startswith("k_w8_gemv<")
+    w8a16_case(capi, "int8", M, K, N, M % 2 == 0, "gemv", outliers=True)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 16, 16), (2, 1040, 1040), (13, 528, 2064), (16, 18944, 64), (17, 3584, 4096),
+                                   (25, 2064, 400), (32, 3600, 4112), (31, 128, 3584)])
+def test_w8a16_e4m3_fp8_path_edges(capi, M, K, N):
+    """Up to 32 tokens E4M3 W8A16 runs as FP8 MMAs on the weight codes against
+    the activations split into two E4M3 terms: both token-tile widths (16, 32)
+    and their ragged tails, K not a multiple of 128 (and K = 16), N not a
+    multiple of the 128-row weight tile, and 1- to 8-way K splits whose partial
+    tiles are summed through the cluster's shared memory."""
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, "e4m3", M, K, N).startswith("k_w8a16_split+k_w8a16_f8<")
+    w8a16_case(capi, "e4m3", M, K, N, M % 2 == 1, "f8", outliers=True)
+
+
+def test_w8a16_e4m3_fp8_path_wide_dynamic_range(capi):
+    """Activations spanning 2^16 within a row: the split keeps every element at
+    least 2^-13.8 of the row's maximum exactly, the rest to 2^-14 of the scale."""
+    M, K, N = 8, 2048, 1024
+    rng = synth.rng_for("test-w8a16", 0, "f8-range", "all")
+    w = synth.weights(N, K, rng)
+    xf = synth.bf16_bits_to_f32(synth.activations(M, K, rng))
+    xf = xf * np.exp2(rng.integers(-16, 1, size=xf.shape)).astype(np.float32)
+    x = synth.f32_to_bf16_bits(xf)
+    q, s = oracle.quantize_weight(oracle.E4M3, w)
+    y = run_w8a16(capi, "e4m3", x, q, s, None)
+    check_tol(y, oracle.w8a16(oracle.E4M3, x, q, s, None), "w8a16 e4m3 wide range")
+
+
 @pytest.mark.parametrize("M", [1, 16])
 def test_w8a16_int8_small_workload(capi, M):
     """INT8 W8A16 single linear K=N=1024, M in {1,16}, full output checked."""
