@@ -39,10 +39,13 @@ using namespace tc;
 namespace {
 
 // ------------------------------------------------------------ activation split
-// One CTA per token row: the row's abs-max, its power-of-two scale, and the two
-// E4M3 terms written into the B-operand layout: token tile j (tt tokens) owns
-// rows [2 tt j, 2 tt j + 2 tt) of xs, x1 of its tokens first, then x2.
-constexpr int kSplitThreads = 256;
+// Token row m, chunk c of kSplitChunk elements: one CTA.  Every CTA of a row
+// reads the whole row for its abs-max (the row is small and L2-resident; all of
+// a thread's loads are issued before any is used) and keeps its own chunk in
+// registers, then writes that chunk's two E4M3 terms into the B-operand
+// layout: token tile j (tt tokens) owns rows [2 tt j, 2 tt j + 2 tt) of xs, x1
+// of its tokens first, then x2.
+constexpr int kSplitThreads = 256, kSplitChunk = 8 * kSplitThreads, kSplitMaxLoads = 16;
 
 // Least power of two s with 448 s >= a (a > 0), from the exponent bits alone:
 // a = f 2^e with f in [1, 2); 448 = 1.75 2^8, so s = 2^(e-8) when f <= 1.75,
@@ -55,22 +58,39 @@ __device__ __forceinline__ float split_scale(float a) {
   return ldexpf(1.0f, max(-126, (e - 1) - (f <= 1.75f ? 8 : 7)));
 }
 
+__device__ __forceinline__ float absmax8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float a = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    a = fmaxf(a, fmaxf(fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)), fabsf(bf16_bits_to_f32(w[e] >> 16))));
+  return a;
+}
+
 __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *__restrict__ x, int M, int K,
                                                                int tt, uint8_t *__restrict__ xs,
                                                                float *__restrict__ xscale) {
   __shared__ float wmax[kSplitThreads / 32];
   pdl_wait();
   pdl_trigger();
-  const int m = blockIdx.x;
+  const int m = blockIdx.y, n8 = K / 8;  // K % 16 == 0
   const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
-  const int n8 = K / 8;  // K % 16 == 0
+  const int mine = blockIdx.x * kSplitThreads + threadIdx.x;  // this thread's 8 elements of the chunk
+  uint4 own = make_uint4(0, 0, 0, 0);
   float a = 0.0f;
-  for (int i = threadIdx.x; i < n8; i += kSplitThreads) {
-    const uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // the whole row, kSplitMaxLoads 16-byte loads in flight per thread at a time
+  for (int base = threadIdx.x; base < n8; base += kSplitThreads * kSplitMaxLoads) {
+    uint4 v[kSplitMaxLoads];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      a = fmaxf(a, fmaxf(fabsf(bf16_bits_to_f32(w[e] & 0xFFFFu)), fabsf(bf16_bits_to_f32(w[e] >> 16))));
+    for (int u = 0; u < kSplitMaxLoads; ++u) {
+      const int i = base + u * kSplitThreads;
+      v[u] = i < n8 ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kSplitMaxLoads; ++u) {
+      a = fmaxf(a, absmax8(v[u]));
+      if (base + u * kSplitThreads == mine) own = v[u];
+    }
   }
   a = warp_max(a);
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = a;
@@ -79,30 +99,26 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
 #pragma unroll
   for (int w = 1; w < kSplitThreads / 32; ++w) a = fmaxf(a, wmax[w]);
   const float s = split_scale(a), r = 1.0f / s;  // powers of two: exact
-  if (threadIdx.x == 0) xscale[m] = s;
+  if (blockIdx.x == 0 && threadIdx.x == 0) xscale[m] = s;
+  if (mine >= n8) return;
   const int j = m / tt, t = m % tt;
   uint8_t *x1 = xs + ((size_t)2 * tt * j + t) * K, *x2 = x1 + (size_t)tt * K;
-  for (int i = threadIdx.x; i < n8; i += kSplitThreads) {
-    const uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t h[4], l[4];  // codes of x1 and x2, two per 16 bits
+  const uint32_t w[4] = {own.x, own.y, own.z, own.w};
+  uint32_t h[4], l[4];  // codes of x1 and x2, two per 16 bits
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float v0 = bf16_bits_to_f32(w[e] & 0xFFFFu) * r, v1 = bf16_bits_to_f32(w[e] >> 16) * r;
-      const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
-      const __half2_raw b1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
-      const float2 f1 = __half22float2(__half2(b1));
-      // the remainders are exact in fp32; times 16 they fit E4M3 (see above)
-      const __nv_fp8x2_storage_t c2 =
-          __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v0 - f1.x), 16.0f * (v1 - f1.y)), __NV_SATFINITE, __NV_E4M3);
-      h[e] = c1;
-      l[e] = c2;
-    }
-    *reinterpret_cast<uint2 *>(x1 + 8 * i) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-    *reinterpret_cast<uint2 *>(x2 + 8 * i) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+  for (int e = 0; e < 4; ++e) {
+    const float v0 = bf16_bits_to_f32(w[e] & 0xFFFFu) * r, v1 = bf16_bits_to_f32(w[e] >> 16) * r;
+    const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+    const float2 f1 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3)));
+    // the remainders are exact in fp32; times 16 they fit E4M3 (see above)
+    const __nv_fp8x2_storage_t c2 =
+        __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v0 - f1.x), 16.0f * (v1 - f1.y)), __NV_SATFINITE, __NV_E4M3);
+    h[e] = c1;
+    l[e] = c2;
   }
+  *reinterpret_cast<uint2 *>(x1 + 8 * mine) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+  *reinterpret_cast<uint2 *>(x2 + 8 * mine) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
 }
-
 
 // ------------------------------------------------------------ the FP8 linear
 // One CTA per (weight tile, token tile, K split).  Warps: 0 = TMA producer,
@@ -116,24 +132,23 @@ template <int TT>  // token tile; the MMA's N is 2 TT (both terms of each token)
 struct W8F8Cfg {
   static constexpr int BM = 128, BK = 128, NB = 2 * TT;
   static constexpr int A_BYTES = BM * BK, B_BYTES = NB * BK, STAGE = A_BYTES + B_BYTES;
-  // about 100 KB of ring, so that two CTAs share an SM and keep the stream busy
-  static constexpr int STAGES = (100 * 1024) / STAGE < 3 ? 3 : (100 * 1024) / STAGE;
-  static constexpr int RING = STAGES * STAGE;
-  static constexpr int PART_BYTES = TT * BM * 4;  // [TT tokens][BM rows] fp32
-  static constexpr int BAR_OFF = RING;
-  static constexpr int SMEM = BAR_OFF + 128 + 1024;
+  // The ring depth is a launch parameter (stages of STAGE bytes; the barriers
+  // follow the ring).
+  static constexpr int MAX_STAGES = 14, BAR_BYTES = 256;
+  static constexpr int PART_BYTES = TT * BM * 4;  // [TT tokens][BM rows] fp32, in the drained ring
   static constexpr int THREADS = 192;
-  static constexpr uint32_t TMEM_COLS = NB;  // 32..256, a power of two
+  static constexpr uint32_t TMEM_COLS = NB;  // 32 or 64, a power of two
   static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, NB);
-  static_assert(PART_BYTES <= RING, "partial tile in the ring");
-  static_assert((2 * STAGES + 1) * 8 + 8 <= 128, "barriers");
+  static constexpr int smem_bytes(int stages) { return stages * STAGE + BAR_BYTES + 1024; }
+  static_assert(PART_BYTES <= 2 * STAGE, "partial tile in a ring of two or more stages");
+  static_assert((2 * MAX_STAGES + 1) * 8 + 8 <= BAR_BYTES, "barriers");
   static_assert(STAGE % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
 
 struct W8F8Params {
   int M, N, K;  // N: output channels (I for the merged gate_up)
   int glu;
-  int ntiles, splits;
+  int ntiles, splits, stages;
   const float *w_scale;
   const float *x_scale;  // per token, from the split
   const uint16_t *bias;
@@ -156,7 +171,8 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   using C = W8F8Cfg<TT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1k(smem_raw);
-  uint64_t *full = (uint64_t *)(smem + C::BAR_OFF), *empty = full + C::STAGES, *acc_full = empty + C::STAGES;
+  const int NS = p.stages;
+  uint64_t *full = (uint64_t *)(smem + NS * C::STAGE), *empty = full + NS, *acc_full = empty + NS;
   uint32_t *tmem_slot = (uint32_t *)(acc_full + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   const int KB = (p.K + C::BK - 1) / C::BK, kb0 = split * KB / S, kb1 = (split + 1) * KB / S, nkb = kb1 - kb0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -191,22 +207,21 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   if (warp == 0) {  // ------------------------------- TMA producer
     if (lane == 0) {
       auto load_w = [&](int i) {
-        uint8_t *st = smem + (i % C::STAGES) * C::STAGE;
+        uint8_t *st = smem + (i % NS) * C::STAGE;
         const int k = (kb0 + i) * C::BK;
         if (p.glu) {  // 64 gate rows, then their 64 up rows
-          tma_load_2d(&tm_w, &full[i % C::STAGES], st, k, tile * 64);
-          tma_load_2d(&tm_w, &full[i % C::STAGES], st + 64 * C::BK, k, p.N + tile * 64);
+          tma_load_2d(&tm_w, &full[i % NS], st, k, tile * 64);
+          tma_load_2d(&tm_w, &full[i % NS], st + 64 * C::BK, k, p.N + tile * 64);
         } else {
-          tma_load_2d(&tm_w, &full[i % C::STAGES], st, k, tile * C::BM);
+          tma_load_2d(&tm_w, &full[i % NS], st, k, tile * C::BM);
         }
       };
       auto load_x = [&](int i) {
-        tma_load_2d(&tm_x, &full[i % C::STAGES], smem + (i % C::STAGES) * C::STAGE + C::A_BYTES,
-                    (kb0 + i) * C::BK, tj * C::NB);
+        tma_load_2d(&tm_x, &full[i % NS], smem + (i % NS) * C::STAGE + C::A_BYTES, (kb0 + i) * C::BK, tj * C::NB);
       };
       // the weights do not depend on the previous kernel of the stream: the first
       // stages' weight tiles are in flight before its split activations are
-      const int pre = nkb < C::STAGES ? nkb : C::STAGES;
+      const int pre = nkb < NS ? nkb : NS;
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], C::STAGE);
         load_w(i);
@@ -215,8 +230,8 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
       for (int i = 0; i < pre; ++i) load_x(i);
       int i = pre;
       for (; i < nkb; ++i) {
-        const int s = i % C::STAGES;
-        if (!mbar_wait(&empty[s], ((i / C::STAGES) & 1) ^ 1, abort_flag)) {
+        const int s = i % NS;
+        if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
           *abort_flag = 1;
           break;
         }
@@ -224,15 +239,15 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
         load_w(i);
         load_x(i);
       }
-      if (*abort_flag) drain_ring(full, C::STAGES, i, C::STAGES);  // armed stages land before the CTA leaves
+      if (*abort_flag) drain_ring(full, NS, i, NS);  // armed stages land before the CTA leaves
     }
   } else if (warp == 1) {  // ------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
       int i = 0;
       for (; i < nkb; ++i) {
-        const int s = i % C::STAGES;
-        if (!mbar_wait(&full[s], (i / C::STAGES) & 1, abort_flag)) {
+        const int s = i % NS;
+        if (!mbar_wait(&full[s], (i / NS) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -246,7 +261,7 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
       }
       if (ok) mma_commit(acc_full);
       // no commit arrival may land after the CTA has left (bounded, also on abort)
-      if (i > 0) ok = mbar_wait_drain(&empty[(i - 1) % C::STAGES], ((i - 1) / C::STAGES) & 1) && ok;
+      if (i > 0) ok = mbar_wait_drain(&empty[(i - 1) % NS], ((i - 1) / NS) & 1) && ok;
       if (!ok) *abort_flag = 1;
     }
   } else {  // ------------------------------------- epilogue: accumulators -> partial tile
@@ -352,7 +367,8 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
   if (!map_u8(&tw, g.qw, g.glu ? 2 * g.N : g.N, g.K, g.glu ? 64 : 128) ||
       !map_u8(&tx, xs, (int64_t)ttiles * C::NB, g.K, C::NB))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_kernel(k_w8a16_split, dim3((unsigned)g.M), dim3(kSplitThreads), 0, st, 1,
+  const int chunks = (int)((g.K + kSplitChunk - 1) / kSplitChunk);
+  cudaError_t e = launch_kernel(k_w8a16_split, dim3((unsigned)chunks, (unsigned)g.M), dim3(kSplitThreads), 0, st, 1,
                                 (const uint16_t *)g.a, (int)g.M, (int)g.K, TT, xs, xscale);
   if (e != cudaSuccess) return e;
   W8F8Params p;
@@ -363,16 +379,21 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
   p.ntiles = g.glu ? (int)(g.N / 64) : (int)((g.N + C::BM - 1) / C::BM);
   const int units = p.ntiles * ttiles, KB = (int)((g.K + C::BK - 1) / C::BK);
   p.splits = w8a16_f8_splits(units, KB, dev.sms);
+  // two CTAs to an SM, each with about 108 KB of ring
+  constexpr int kShared = 108 * 1024;
+  constexpr int max_stages = kShared / C::STAGE < C::MAX_STAGES ? kShared / C::STAGE : C::MAX_STAGES;
+  p.stages = max_stages;
   p.w_scale = g.w_scale;
   p.x_scale = xscale;
   p.bias = g.bias;
   p.y = (uint16_t *)g.y;
   p.status = dev.status;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(k_w8a16_f8<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static_assert(C::smem_bytes(max_stages) <= 227 * 1024, "shared memory");
+  static const cudaError_t attr = cudaFuncSetAttribute(k_w8a16_f8<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       C::smem_bytes(max_stages));
   if (attr != cudaSuccess) return attr;
-  return launch_kernel(k_w8a16_f8<TT>, dim3((unsigned)units, 1, (unsigned)p.splits), dim3(C::THREADS), C::SMEM,
-                       st, (unsigned)p.splits, tw, tx, p);
+  return launch_kernel(k_w8a16_f8<TT>, dim3((unsigned)units, 1, (unsigned)p.splits), dim3(C::THREADS),
+                       C::smem_bytes(p.stages), st, (unsigned)p.splits, tw, tx, p);
 }
 
 }  // namespace
@@ -382,11 +403,13 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
 // and the BF16 path with converted weights is faster.
 int w8a16_f8_tt(int64_t M) { return M <= 16 ? 16 : 32; }
 
-// K splits (a cluster of at most 8 CTAs): the fewest that put a CTA on every
-// SM, keeping at least 4 k-blocks of 128 per CTA.
+// K splits (a cluster of at most 8 CTAs): as many as fit two CTAs to an SM,
+// and at least 4 k-blocks of 128 per CTA.  A CTA's stream rate is bounded by
+// its own rate of issue more than by its ring depth (measured: 5 and 11 stages
+// stream alike), so more CTAs beat deeper rings.
 int w8a16_f8_splits(int units, int kblocks, int sms) {
   int s = 1;
-  while (s < 8 && units * s < sms && kblocks / (s + 1) >= 4) ++s;
+  while (s < 8 && units * (s + 1) <= 2 * sms && kblocks / (s + 1) >= 4) ++s;
   return s;
 }
 
