@@ -140,12 +140,6 @@ int w8a16_f8_splits(int units, int kblocks, int sms);
 size_t w8a16_f8_workspace(int64_t M, int64_t K);
 cudaError_t launch_w8a16_f8(const GemmArgs &g, void *ws, const DeviceInfo &dev, cudaStream_t st);
 
-// Small-batch W8A16 on the CUDA cores (gemv.cu): M <= kW8GemvMaxM tokens,
-// plain or merged gate_up.
-constexpr int kW8GemvMaxM = 8;
-cudaError_t launch_w8_gemv(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
-int w8_gemv_splits(int64_t N, int glu, int sms);
-
 // Fused-quantization FP8 GEMM: task-flag area (u32) for these sizes, and
 // whether the fused kernel is used.
 size_t fp8_xq_flag_bytes(int64_t M, int64_t K);

@@ -107,10 +107,6 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
       if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) {
         return w8a16_f8_tt(M) == 16 ? "k_w8a16_split+k_w8a16_f8<16>" : "k_w8a16_split+k_w8a16_f8<32>";
       }
-      if (M <= kW8GemvMaxM) {
-        static const char *gv[4] = {"k_w8_gemv<1>", "k_w8_gemv<2>", "k_w8_gemv<4>", "k_w8_gemv<8>"};
-        return gv[M <= 1 ? 0 : M <= 2 ? 1 : M <= 4 ? 2 : 3];
-      }
       static const char *names[5] = {"k_w8_dq<16>", "k_w8_dq<32>", "k_w8_dq<64>", "k_w8_dq<128>", "k_w8_dq<256>"};
       const int b = w8_swap_bnt(M, N, K, sm_count());
       return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : b == 128 ? 3 : 4];
@@ -249,8 +245,6 @@ qlin_status qlin_w8a16_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N,
   GemmArgs g{kW8A16, qtype, M, K, N, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
   // E4M3 weights, small batch: FP8 MMAs on the codes against the split activations
   if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) return from_cuda(launch_w8a16_f8(g, ws, *dev, (cudaStream_t)stream));
-  // INT8 weights, a handful of tokens: a weight-streaming matrix-vector product on the CUDA cores
-  if (M <= kW8GemvMaxM) return from_cuda(launch_w8_gemv(g, *dev, (cudaStream_t)stream));
   return from_cuda(launch_w8a16_swap(g, *dev, (cudaStream_t)stream));
 }
 
@@ -350,7 +344,6 @@ qlin_status qlin_w8a16_gate_up_silu(qlin_qtype qtype, int64_t M, int64_t K, int6
   GemmArgs g{kW8A16, qtype, M, K, I, x, qw, w_scale, nullptr, (const uint16_t *)bias, y};
   g.glu = 1;
   if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) return from_cuda(launch_w8a16_f8(g, ws, *dev, (cudaStream_t)stream));
-  if (M <= kW8GemvMaxM) return from_cuda(launch_w8_gemv(g, *dev, (cudaStream_t)stream));
   return from_cuda(launch_w8a16_swap(g, *dev, (cudaStream_t)stream));
 }
 

@@ -102,11 +102,7 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert L.qlin_w8a8_gate_up_silu(1, 4, 64, 128, good, good, good, good, None, good, None, 0, None) == WS
     assert L.qlin_w8a8_gate_up_silu(1, 4, 64, 100, good, good, good, good, None, good, good, 4096, None) == INV
     assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A8_GATE_UP_SILU, "e4m3", 4, 64, 128) >= 256
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_GATE_UP_SILU, 0, 1, 3584, 18944) == "k_w8_gemv<1>"
-    # up to 8 tokens the W8A16 layer is a CUDA-core matrix-vector product; from 9 the tensor-core kernel
-    for m, name in [(1, "k_w8_gemv<1>"), (2, "k_w8_gemv<2>"), (3, "k_w8_gemv<4>"), (5, "k_w8_gemv<8>"),
-                    (8, "k_w8_gemv<8>"), (9, "k_w8_dq<16>")]:
-        assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, 0, m, 3584, 3584) == name
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_GATE_UP_SILU, 0, 1, 3584, 18944) == "k_w8_dq<16>"
     # E4M3 weights up to 128 tokens: FP8 MMAs against the split activations; above, the BF16 path
     for m, name in [(1, "k_w8a16_split+k_w8a16_f8<16>"), (16, "k_w8a16_split+k_w8a16_f8<16>"),
                     (17, "k_w8a16_split+k_w8a16_f8<32>"), (32, "k_w8a16_split+k_w8a16_f8<32>"),

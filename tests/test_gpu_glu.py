@@ -70,14 +70,6 @@ def test_w8a16_gate_up_silu(capi, qt, M, K, I):
     w8a16_glu(capi, qt, M, K, I, M % 2 == 0, "a")
 
 
-@pytest.mark.parametrize("M,K,I", [(2, 1040, 384), (5, 3584, 128), (8, 528, 2048)])
-def test_w8a16_gate_up_silu_int8_cuda_core_path(capi, M, K, I):
-    """Up to 8 tokens the INT8 merged gate_up runs on the CUDA cores: gate row n
-    and up row I + n go through one warp, and silu(g) * u is formed before the store."""
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_GATE_UP_SILU, "int8", M, K, I).startswith("k_w8_gemv<")
-    w8a16_glu(capi, "int8", M, K, I, M % 2 == 1, "gemv")
-
-
 @pytest.mark.parametrize("M,K,I", [(1, 1040, 384), (16, 3584, 128), (29, 528, 2048), (32, 2048, 640)])
 def test_w8a16_gate_up_silu_e4m3_fp8_path(capi, M, K, I):
     """E4M3 up to 32 tokens: a weight tile is 64 gate rows and their 64 up rows,

@@ -71,17 +71,6 @@ def test_w8a16_ragged_kn(capi, qt, M, K, N):
     w8a16_case(capi, qt, M, K, N, M % 2 == 1, "ragged-kn", outliers=True)
 
 
-@pytest.mark.parametrize("M,K,N", [(4, 1040, 1040), (6, 528, 2064), (7, 18944, 64), (2, 3584, 9472), (8, 16, 4096),
-                                   (1, 2064, 32), (3, 3600, 4112)])
-def test_w8a16_int8_cuda_core_path_edges(capi, M, K, N):
-    """Up to 8 tokens INT8 W8A16 runs as a matrix-vector product on the CUDA
-    cores: token counts below the kernel's template width, K not a multiple of
-    its 512-code step (and K = 16), and few output rows, where K is split over 2
-    or 4 warps whose partial sums meet in shared memory."""
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, "int8", M, K, N).startswith("k_w8_gemv<")
-    w8a16_case(capi, "int8", M, K, N, M % 2 == 0, "gemv", outliers=True)
-
-
 @pytest.mark.parametrize("M,K,N", [(1, 16, 16), (2, 1040, 1040), (13, 528, 2064), (16, 18944, 64), (17, 3584, 4096),
                                    (25, 2064, 400), (32, 3600, 4112), (31, 128, 3584)])
 def test_w8a16_e4m3_fp8_path_edges(capi, M, K, N):
