@@ -116,10 +116,12 @@ struct Fp8CfgT {
   static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages : 4;
   static constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
   // epilogue: one 32 x 32 BF16 block per epilogue warp, staged for a TMA store
-  static constexpr int EPI_OFF = STAGES * STAGE_BYTES, EPI_WARP_BYTES = 32 * 32 * 2, EPI_BYTES = 8 * EPI_WARP_BYTES;
+  // (XQ: stored directly by rows, the shared memory holds the activation ring)
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES, EPI_WARP_BYTES = 32 * 32 * 2;
+  static constexpr int EPI_BYTES = XQ ? 0 : 8 * EPI_WARP_BYTES;
   // XQ: a ring of chunks (XQ_ROWS rows of a task's 128 x 128 BF16 activation
   // tile), TMA-staged, as many as the rest of the shared memory holds
-  static constexpr int XQ_ROWS = 32, XQ_CPT = BM / XQ_ROWS, XQ_CHUNK = XQ_ROWS * BK * 2;
+  static constexpr int XQ_ROWS = 64, XQ_CPT = BM / XQ_ROWS, XQ_CHUNK = XQ_ROWS * BK * 2;
   static constexpr int XQ_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int XQ_NBUF = XQ ? (227 * 1024 - XQ_OFF - 256 - 1024) / XQ_CHUNK : 0;
   static constexpr int BAR_OFF = XQ_OFF + XQ_NBUF * XQ_CHUNK;
@@ -468,6 +470,16 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     const uint32_t st_row = smem_u32(stage) + 64u * lane, sw = (lane >> 1) & 3;
     bool pending = false;  // lane 0 has a store in flight that reads the staging block
     auto emit = [&](const uint32_t (&o)[16], int x, int y) {
+      if constexpr (XQ == 1) {  // row stores: lane = row y + lane, columns x..x+31 (64 bytes)
+        const int m = y + lane;
+        if (m < p.M) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.y + (size_t)m * p.N + x);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (x + 8 * g < p.N) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+        }
+        return;
+      }
       if (pending) {
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
@@ -1371,25 +1383,25 @@ size_t fp8_xq_flag_bytes(int64_t M, int64_t K) {
   return (size_t)(mtiles * ((nkb + 3) / 4 * 4 + 1) * 4);
 }
 
-// The fused kernel pays a start-up of one quantization task before the first
-// tiles can load, and its quantizer shares the SMs' shared-memory bandwidth
-// with the GEMM.  It wins where the activations are many (16 m-tiles and up)
-// and each GEMM row is short (at most 4096 columns, so the quantization is a
-// large share of the work); on wider GEMMs the separate quantization pass is as
-// fast or faster.  Its quantizers are the GEMM's CTAs, so the tile pairs must
-// fill every SM.  N counts GEMM columns (2I for the merged gate_up).
+// The fused kernel hides the quantization behind the GEMM's main loop, but its
+// shared memory holds the activation ring instead of the staging that lets the
+// separate GEMM store its outputs through TMA.  Measured, it wins where each
+// tile's main loop is long and the quantization a large share of the work:
+// K >= 4096, at most 4096 GEMM columns, and 64 m-tiles or more (8192 tokens);
+// at K = 2048 the separate pass with the TMA-store epilogue is 20-28% faster.
+// Its quantizers are the GEMM's CTAs, so the tile pairs must fill every SM.
+// N counts GEMM columns (2I for the merged gate_up).
 // QLIN_FP8_FUSED_QUANT=0 in the environment (read once) keeps the separate
 // quantization pass everywhere: a profiler that re-issues cooperative launches
 // without their cluster shape cannot run the fused kernel.
 bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms) {
-  (void)K;
   static const bool enabled = [] {
     const char *v = std::getenv("QLIN_FP8_FUSED_QUANT");
     return !(v && v[0] == '0' && v[1] == 0);
   }();
   if (!enabled) return false;
   const int64_t mtiles = (M + Fp8Cfg::BM - 1) / Fp8Cfg::BM, ntiles = (N + Fp8Cfg::BN - 1) / Fp8Cfg::BN;
-  return mtiles >= 16 && N <= 4096 && ((mtiles + 1) / 2) * ntiles >= sms / 2;
+  return mtiles >= 64 && K >= 4096 && N <= 4096 && ((mtiles + 1) / 2) * ntiles >= sms / 2;
 }
 
 int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms) {

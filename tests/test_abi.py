@@ -112,12 +112,14 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A16_LINEAR, "int8", 1, 3584, 3584) == 0
     assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A16_LINEAR, "e4m3", 33, 3584, 3584) == 0
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 11008) == "k_quantize_act+k_fp8_gemm"
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 2048) == "k_fp8_gemm<xq>"
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 4096) == "k_fp8_gemm<xq>"
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 4112) == "k_quantize_act+k_fp8_gemm"
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 1920, 2048, 2048) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 4096, 1024) == "k_fp8_gemm<xq>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 11008, 2048) == "k_fp8_gemm<xq>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 4096, 4096) == "k_fp8_gemm<xq>"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 4096, 4112) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 2048) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8064, 11008, 2048) == "k_quantize_act+k_fp8_gemm"
     # one n-tile: the pairs would not fill the SMs
-    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 256) == "k_quantize_act+k_fp8_gemm"
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 11008, 256) == "k_quantize_act+k_fp8_gemm"
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 1024, 2048, 11008) == "k_quantize_act+k_fp8_gemm"
 
 
@@ -138,8 +140,8 @@ def test_fused_quant_switch_selects_the_separate_pass():
     import subprocess
     import sys
     code = ("from bit_quantized_linear_gb300 import capi; "
-            "print(capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 2048)); "
-            "print(capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 2048, 1024))")
+            "print(capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 11008, 2048)); "
+            "print(capi.qlin_kernel_name(capi.QLIN_OP_W8A8_GATE_UP_SILU, 1, 8192, 4096, 1024))")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = dict(os.environ, QLIN_FP8_FUSED_QUANT="0", PYTHONPATH=root)
     out = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True, text=True,

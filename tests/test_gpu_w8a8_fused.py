@@ -86,8 +86,8 @@ def test_fused_int8_gate_up_silu(capi):
 
 
 # ---------------------------------------------------------------- FP8 (E4M3)
-# From 16 token tiles (M > 1920), for GEMMs of at most 4096 columns whose tile
-# pairs fill the SMs, the E4M3 W8A8 linear is one kernel too: warps of every
+# From 64 token tiles (M > 8064), K >= 4096, for GEMMs of at most 4096 columns
+# whose tile pairs fill the SMs, the E4M3 W8A8 linear is one kernel too: warps of every
 # GEMM CTA quantize the activations into the codes workspace, task by task, and
 # the TMA producer waits on each task's flag (or its band's count) before
 # loading those codes, so the quantization overlaps the tensor-core work.
@@ -117,21 +117,21 @@ def _run_e4m3(capi, M, K, N, tag, x_scale_mult=1.0, with_bias=False, glu=False):
     check_tol(from_dev_bf16(y)[rows], ref, f"fused e4m3 {M}x{K}x{N} {tag}")
 
 
-@pytest.mark.parametrize("M,K,N", [(2560, 2048, 2048), (2561, 1024, 2304), (2600, 2064, 2048), (4096, 16, 2560),
-                                   (2560, 11008, 2048)])
+@pytest.mark.parametrize("M,K,N", [(8192, 4096, 2048), (8193, 4112, 2304), (8200, 4224, 1024),
+                                   (8192, 11008, 2048)])
 def test_fused_e4m3_w8a8_shapes(capi, M, K, N):
     _run_e4m3(capi, M, K, N, "shapes", with_bias=(K % 128 != 0))
 
 
 def test_fused_e4m3_w8a8_beyond_calibration_range(capi):
-    _run_e4m3(capi, 2304, 1024, 4096, "clamp", x_scale_mult=40.0)
+    _run_e4m3(capi, 8320, 4096, 4096, "clamp", x_scale_mult=40.0)
 
 
 def test_fused_e4m3_gate_up_silu(capi):
-    _run_e4m3(capi, 2560, 2048, 1024, "glu", glu=True, with_bias=True)
+    _run_e4m3(capi, 8192, 4096, 1024, "glu", glu=True, with_bias=True)
 
 
-@pytest.mark.parametrize("M,K,N", [(2433, 2064, 2048), (4096, 16, 2048), (2400, 1040, 4096)])
+@pytest.mark.parametrize("M,K,N", [(8193, 4112, 2048), (8320, 4096, 4096)])
 def test_fused_e4m3_codes_bitexact(capi, M, K, N):
     """The in-GEMM quantizer leaves its codes in the workspace's first M*K bytes:
     they must equal the oracle's static E4M3 quantization bit for bit, here with
