@@ -487,10 +487,12 @@ class KvWorkload(GpuWorkload):
                                    f"{L2_BYTES / 2**20:.0f} MiB)"}
 
 
-def kernel_digest() -> str:
+def kernel_digest(files=None) -> str:
+    """Digest of the kernel sources in `files` (names under csrc/; all of them
+    when None)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "bit_quantized_linear_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files if files is not None else os.listdir(d)):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -505,7 +507,8 @@ def traffic_for(kernel: str, wl: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{wl}:{kernel}")
-    if not e or e.get("kernel_digest") != kernel_digest():
+    # the digest covers the sources the call's kernels are built from
+    if not e or e.get("kernel_digest") != kernel_digest(e.get("digest_files")):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -71,8 +71,12 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
                                                                int tt, uint8_t *__restrict__ xs,
                                                                float *__restrict__ xscale) {
   __shared__ float wmax[kSplitThreads / 32];
-  pdl_wait();
+  // The FP8 linear that follows may start at once: before its own wait for this
+  // kernel it only arms barriers and loads weight tiles, so its CTAs take the
+  // SMs that the previous linear frees during its tail.  Nothing here is
+  // written before the previous kernel has completed.
   pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.y, n8 = K / 8;  // K % 16 == 0
   const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
   const int mine = blockIdx.x * kSplitThreads + threadIdx.x;  // this thread's 8 elements of the chunk
@@ -219,19 +223,26 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
       auto load_x = [&](int i) {
         tma_load_2d(&tm_x, &full[i % NS], smem + (i % NS) * C::STAGE + C::A_BYTES, (kb0 + i) * C::BK, tj * C::NB);
       };
-      // the weights do not depend on the previous kernel of the stream: the first
-      // stages' weight tiles are in flight before its split activations are
+      // Before the wait for the split (and, through it, for every earlier kernel
+      // of the stream) only L2 prefetches of the first weight tiles are issued.
+      // An earlier kernel may still be writing these weights, and a prefetch into
+      // the coherent L2 cannot hand a stale byte to the MMAs.  Every load into
+      // shared memory follows the wait.
       const int pre = nkb < NS ? nkb : NS;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], C::STAGE);
-        load_w(i);
+        const int k = (kb0 + i) * C::BK;
+        if (p.glu) {
+          tma_prefetch_l2_2d(&tm_w, k, tile * 64);
+          tma_prefetch_l2_2d(&tm_w, k, p.N + tile * 64);
+        } else {
+          tma_prefetch_l2_2d(&tm_w, k, tile * C::BM);
+        }
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) load_x(i);
-      int i = pre;
+      int i = 0;
       for (; i < nkb; ++i) {
         const int s = i % NS;
-        if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
+        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
           *abort_flag = 1;
           break;
         }
