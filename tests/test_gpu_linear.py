@@ -83,31 +83,32 @@ def test_w8a16_e4m3_fp8_path_edges(capi, M, K, N):
     w8a16_case(capi, "e4m3", M, K, N, M % 2 == 1, "f8", outliers=True)
 
 
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
 @pytest.mark.parametrize("M", [1, 32, 128])
-def test_w8a16_reads_weights_quantized_just_before(capi, M):
+def test_w8a16_reads_weights_quantized_just_before(capi, qt, M):
     """Stream order: the weight codes that the kernel right before the linear
     writes on the device (same buffers, no synchronisation in between) are the
-    codes the linear reads.  The FP8 path lets each call's weight traffic start
-    during the previous kernel's tail; only L2 prefetches run before its wait, so
-    no stale code reaches the tensor cores."""
+    codes the linear reads.  The linears let their weight traffic start during
+    the previous kernel's tail; only L2 prefetches run before their wait, so no
+    stale code reaches the tensor cores."""
     K, N = 3584, 4096
-    rng = synth.rng_for("test-w8a16", 0, f"stream-order-{M}", "all")
+    rng = synth.rng_for("test-w8a16", 0, f"stream-order-{qt}-{M}", "all")
     w_old, w_new = synth.weights(N, K, rng), synth.weights(N, K, rng)
     x = synth.activations(M, K, rng)
     wd_old, wd_new, xd = to_dev(w_old), to_dev(w_new), to_dev_bf16(x)
     qw = torch.empty((N, K), dtype=torch.uint8, device="cuda")
     s = torch.empty((N,), dtype=torch.float32, device="cuda")
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    ws = capi.workspace(capi.QLIN_OP_W8A16_LINEAR, "e4m3", M, K, N)
+    ws = capi.workspace(capi.QLIN_OP_W8A16_LINEAR, qt, M, K, N)
     for _ in range(4):
-        capi.qlin_quantize_weight("e4m3", wd_old, qw, s)
-        capi.qlin_w8a16_linear("e4m3", xd, qw, s, None, y, ws)
-        capi.qlin_quantize_weight("e4m3", wd_new, qw, s)
-        capi.qlin_w8a16_linear("e4m3", xd, qw, s, None, y, ws)
+        capi.qlin_quantize_weight(qt, wd_old, qw, s)
+        capi.qlin_w8a16_linear(qt, xd, qw, s, None, y, ws)
+        capi.qlin_quantize_weight(qt, wd_new, qw, s)
+        capi.qlin_w8a16_linear(qt, xd, qw, s, None, y, ws)
     torch.cuda.synchronize()
     assert capi.qlin_get_device_status() == capi.QLIN_OK
-    q, sc = oracle.quantize_weight(oracle.E4M3, w_new)
-    check_tol(from_dev_bf16(y), oracle.w8a16(oracle.E4M3, x, q, sc, None), f"w8a16 stream order M={M}")
+    q, sc = oracle.quantize_weight(QT[qt], w_new)
+    check_tol(from_dev_bf16(y), oracle.w8a16(QT[qt], x, q, sc, None), f"w8a16 {qt} stream order M={M}")
 
 
 def test_w8a16_e4m3_fp8_path_wide_dynamic_range(capi):
