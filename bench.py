@@ -254,8 +254,8 @@ class GpuWorkload:
             # one device buffer (and one pinned host mirror) for all of a step's
             # activations, and one for all of its outputs: the end-to-end step
             # moves each with a single copy, as a caller batching a step would
-            self.x, self.x_flat, self.x_host_flat = self._pack(self.x, dev, fill=True)
-            self.y, self.y_flat, self.y_host_flat = self._pack(self.y, dev, fill=False)
+            self.x, self.x_flat, self.x_host_flat, self.x_offs = self._pack(self.x, dev, fill=True)
+            self.y, self.y_flat, self.y_host_flat, self.y_offs = self._pack(self.y, dev, fill=False)
         torch.cuda.synchronize()
         P = ctypes.c_void_p
 
@@ -308,7 +308,7 @@ class GpuWorkload:
                 v.copy_(t)
                 host[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
             views.append(v)
-        return views, flat, host
+        return views, flat, host, offs
 
     def set_accounting(self):
         """Per-call algorithmic bytes / flops, the tensor peak each call is bound by,
@@ -318,12 +318,34 @@ class GpuWorkload:
         self.call_fp8 = [l.form == "w8a8" and l.qtype == "e4m3" for l in self.lins]
         self.call_info = [{"name": l.name, "M": l.M, "K": l.K, "N": l.N, **({"out": out_cols(l)} if l.glu else {})}
                           for l in self.lins]
-        if self.packed:
-            self.h2d = [(self.x_flat, self.x_host_flat)]
-            self.d2h = [(self.y_host_flat, self.y_flat)]
-        else:
-            self.h2d = [(self.x[i], self.x_host[i]) for i in range(len(self.lins))]
-            self.d2h = [(self.y_host[i], self.y[i]) for i in range(len(self.lins))]
+        # End-to-end copy groups: runs of calls with one batch size and at most
+        # 4 MB of activations.  A group's inputs come in ahead of its calls and
+        # its outputs go back while the later calls run, as a caller that
+        # pipelines its transfers would do; every byte is still moved each step.
+        bounds, g0, gbytes = [], 0, 0
+        for i, l in enumerate(self.lins):
+            xb = l.M * l.K * 2
+            if i > g0 and (l.M != self.lins[g0].M or gbytes + xb > 4 << 20):
+                bounds.append((g0, i))
+                g0, gbytes = i, 0
+            gbytes += xb
+        bounds.append((g0, len(self.lins)))
+
+        def span(ts, offs, i0, i1):  # bytes [first, last) of calls i0..i1-1 in a packed buffer
+            return offs[i0], offs[i1 - 1] + ts[i1 - 1].numel() * ts[i1 - 1].element_size()
+        self.e2e_groups = []
+        for i0, i1 in bounds:
+            if self.packed:
+                a, b = span(self.x, self.x_offs, i0, i1)
+                c, d = span(self.y, self.y_offs, i0, i1)
+                h2d = [(self.x_flat[a:b], self.x_host_flat[a:b])]
+                d2h = [(self.y_host_flat[c:d], self.y_flat[c:d])]
+            else:
+                h2d = [(self.x[i], self.x_host[i]) for i in range(i0, i1)]
+                d2h = [(self.y_host[i], self.y[i]) for i in range(i0, i1)]
+            self.e2e_groups.append((i0, i1, h2d, d2h))
+        self.h2d = [c for grp in self.e2e_groups for c in grp[2]]
+        self.d2h = [c for grp in self.e2e_groups for c in grp[3]]
         l0 = self.lins[0]
         self.dtype = (("e4m3" if l0.qtype == "e4m3" else "int8") + ("xbf16" if l0.form == "w8a16" else "")
                       + "->f32acc->bf16")
@@ -340,22 +362,52 @@ class GpuWorkload:
         name), just the calls that launch that kernel, in step order."""
         torch = self.torch
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=self.stream):
-            if e2e:
+        groups = getattr(self, "e2e_groups", None) if e2e else None
+        main = self.stream
+        with torch.cuda.graph(g, stream=main):
+            in_ev, starts, ends = [], {}, {}
+            if groups is not None:  # inputs on one copy stream, outputs on another
+                fork = torch.cuda.Event()
+                fork.record(main)
+                self.cp_in.wait_event(fork)
+                self.cp_out.wait_event(fork)
+                with torch.cuda.stream(self.cp_in):
+                    for k, (i0, i1, h2d, _) in enumerate(groups):
+                        for dst, src in h2d:
+                            dst.copy_(src, non_blocking=True)
+                        e = torch.cuda.Event()
+                        e.record(self.cp_in)
+                        in_ev.append(e)
+                        starts[i0], ends[i1 - 1] = k, k
+            elif e2e:
                 for dst, src in self.h2d:
                     dst.copy_(src, non_blocking=True)
             args = self.args[copy]
             for i, fn in enumerate(self.fns):
                 if only is not None and self.kernel[i] != only:
                     continue
+                if i in starts:
+                    main.wait_event(in_ev[starts[i]])
                 if events is not None:
-                    events[i][0].record(self.stream)
+                    events[i][0].record(main)
                 st = fn(*args[i])
                 if events is not None:
-                    events[i][1].record(self.stream)
+                    events[i][1].record(main)
                 if st != 0:
                     raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
-            if e2e:
+                if i in ends:
+                    e = torch.cuda.Event()
+                    e.record(main)
+                    self.cp_out.wait_event(e)
+                    with torch.cuda.stream(self.cp_out):
+                        for dst, src in groups[ends[i]][3]:
+                            dst.copy_(src, non_blocking=True)
+            if groups is not None:  # both copy streams rejoin before the step ends
+                for side in (self.cp_in, self.cp_out):
+                    e = torch.cuda.Event()
+                    e.record(side)
+                    main.wait_event(e)
+            elif e2e:
                 for dst, src in self.d2h:
                     dst.copy_(src, non_blocking=True)
         return g
@@ -364,6 +416,7 @@ class GpuWorkload:
         torch = self.torch
         # capture on a side stream; the pre-marshalled stream argument must be the capture stream
         self.stream = torch.cuda.Stream()
+        self.cp_in, self.cp_out = torch.cuda.Stream(), torch.cuda.Stream()
         sp = ctypes.c_void_p(self.stream.cuda_stream)
         self.args = [[a[:-1] + (sp,) for a in argset] for argset in self.args]
         torch.cuda.synchronize()
@@ -387,13 +440,6 @@ class GpuWorkload:
                 ev[i][1].record(self.stream)
             if st != 0:
                 raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
-
-    def run_step_e2e(self, step):
-        for dst, src in self.h2d:
-            dst.copy_(src, non_blocking=True)
-        self.run_step(step)
-        for dst, src in self.d2h:
-            dst.copy_(src, non_blocking=True)
 
 
 def kv_bytes(T, H, D, store):
@@ -824,7 +870,10 @@ def main():
         e2e = {"value": whole_job_value(units_step, a.steps, world, et, unit_scale), "unit": metric_unit,
                "h2d_bytes_per_step": int(sum(src.numel() * src.element_size() for _, src in W.h2d)),
                "d2h_bytes_per_step": int(sum(src.numel() * src.element_size() for _, src in W.d2h)),
-               "how": "CUDA-graph replay: pinned-host inputs copied in, the step's kernels, outputs copied out"}
+               "how": ("CUDA-graph replay: pinned-host inputs copied in and outputs copied out every step; "
+                       "each group of calls waits only for its own inputs, and its outputs go back while "
+                       "later calls run" if getattr(W, "e2e_groups", None) else
+                       "CUDA-graph replay: pinned-host inputs copied in, the step's kernels, outputs copied out")}
 
     stream_ctx.__exit__(None, None, None)
     cpu = None
