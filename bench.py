@@ -395,7 +395,7 @@ class GpuWorkload:
                     events[i][1].record(main)
                 if st != 0:
                     raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
-                if i in ends:
+                if i in ends and groups[ends[i]][3]:
                     e = torch.cuda.Event()
                     e.record(main)
                     self.cp_out.wait_event(e)
@@ -520,10 +520,14 @@ class KvWorkload(GpuWorkload):
             self.call_info.append({"name": f"L{layer}.kv_load", "T": S, "H": H, "D": D})
         self.call_flops = [0] * len(self.fns)
         self.call_fp8 = [False] * len(self.fns)
-        # e2e: the new tokens come from the host; the last layer's dequantized context goes back
-        self.h2d = [(self.k_new[i], self.k_new_host[i]) for i in range(synth.KV_LAYERS)] + \
-                   [(self.v_new[i], self.v_new_host[i]) for i in range(synth.KV_LAYERS)]
-        self.d2h = [(self.k_out_host, self.k_out), (self.v_out_host, self.v_out)]
+        # e2e: the new tokens come from the host, each layer's ahead of its calls;
+        # the last layer's dequantized context goes back
+        nl = synth.KV_LAYERS
+        self.e2e_groups = [(2 * i, 2 * i + 2, [(self.k_new[i], self.k_new_host[i]), (self.v_new[i], self.v_new_host[i])],
+                            [(self.k_out_host, self.k_out), (self.v_out_host, self.v_out)] if i == nl - 1 else [])
+                           for i in range(nl)]
+        self.h2d = [c for grp in self.e2e_groups for c in grp[2]]
+        self.d2h = [c for grp in self.e2e_groups for c in grp[3]]
         self.dtype = "bf16->int8|e4m3 codes+f16 scales->bf16"
         cache_bytes = sum(a.numel() * a.element_size() for c in self.caches for a in c)
         self.weight_bytes = cache_bytes
