@@ -322,14 +322,7 @@ class GpuWorkload:
         # 4 MB of activations.  A group's inputs come in ahead of its calls and
         # its outputs go back while the later calls run, as a caller that
         # pipelines its transfers would do; every byte is still moved each step.
-        bounds, g0, gbytes = [], 0, 0
-        for i, l in enumerate(self.lins):
-            xb = l.M * l.K * 2
-            if i > g0 and (l.M != self.lins[g0].M or gbytes + xb > 4 << 20):
-                bounds.append((g0, i))
-                g0, gbytes = i, 0
-            gbytes += xb
-        bounds.append((g0, len(self.lins)))
+        bounds = e2e_group_bounds([(l.M, l.M * l.K * 2) for l in self.lins])
 
         def span(ts, offs, i0, i1):  # bytes [first, last) of calls i0..i1-1 in a packed buffer
             return offs[i0], offs[i1 - 1] + ts[i1 - 1].numel() * ts[i1 - 1].element_size()
@@ -440,6 +433,22 @@ class GpuWorkload:
                 ev[i][1].record(self.stream)
             if st != 0:
                 raise RuntimeError(f"{self.kernel[i]}: status {self.capi.status_string(st)}")
+
+
+def e2e_group_bounds(calls, cap=4 << 20):
+    """[(first, end)] index ranges that split calls, given as (batch size,
+    activation bytes) in step order, into runs of one batch size whose
+    activations total at most `cap` bytes (a call larger than `cap` is a group
+    of its own)."""
+    bounds, g0, gbytes = [], 0, 0
+    for i, (m, xb) in enumerate(calls):
+        if i > g0 and (m != calls[g0][0] or gbytes + xb > cap):
+            bounds.append((g0, i))
+            g0, gbytes = i, 0
+        gbytes += xb
+    if calls:
+        bounds.append((g0, len(calls)))
+    return bounds
 
 
 def kv_bytes(T, H, D, store):
