@@ -28,6 +28,12 @@
  *   - Every call is asynchronous on `stream` (NULL = legacy default stream) and
  *     returns once the work is enqueued.  Only qlin_get_device_status()
  *     synchronizes.
+ *   - Calls on one stream are ordered like any work on it.  A call sees
+ *     everything earlier work on the stream wrote, weights included, and
+ *     later work sees its outputs.  Consecutive kernels of the library start
+ *     early (programmatic dependent launch).  Before a kernel's wait for its
+ *     predecessor it only prefetches weights into the coherent L2, so an
+ *     overlapping predecessor can never make it read stale data.
  *   - Argument errors are detected on the host before anything is launched and
  *     returned as a status: NULL required pointer, negative sizes, K or N not a
  *     multiple of 16, pointers not 16-byte aligned, unknown qtype, workspace
