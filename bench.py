@@ -9,14 +9,22 @@ bytes (8-bit weights + fp32 scales + BF16 activations in + BF16 outputs out).
 Two copies of the weights (2 x 217 MB, each larger than the 129 MB L2)
 alternate between steps, so every step streams its weights from HBM.
 
-Other workloads (--workload): small, w8a8-3b, prefill, stack-decode,
-stack-prefill; prefill-shaped ones report TFLOP/s instead of GB/s.
+The default run also times the FP8-E4M3 W8A8 static prefill workload (M in
+{1024, 4096, 16384, 32640} x (K, N) in {(2048, 11008), (11008, 2048),
+(2048, 2048)}) and reports it, in TFLOP/s against the FP8 tensor peak, as the
+line's "prefill" object with its own roofline, CPU baseline, end-to-end figure
+and clocks (--no-prefill skips it).
+
+Other workloads (--workload): small, w8a8-3b, w8a8-dyn-3b, prefill,
+stack-decode, stack-prefill, stack-fused-decode, stack-fused-prefill, kv7b;
+prefill-shaped ones report TFLOP/s instead of GB/s.
 
 --impl reference times the CPU oracle (the plain fp64 restatement of the layer)
 on a bounded sample of the same workload on the host cores.
 
 Under torchrun (--gpus N > 1) every rank runs an independent replica (the layer
-has no exchange step); value is the sum over ranks of units / max elapsed.
+has no exchange step); value is the sum over ranks of units / max elapsed.  The
+ranks meet only in a host-side gloo group (barriers and one max reduction).
 Prints one JSON line on rank 0.
 """
 from __future__ import annotations
@@ -653,14 +661,15 @@ def cpu_baseline(name, unit_scale, unit):
 
 
 # ------------------------------------------------------- replicas (N > 1)
-def max_over_ranks(value: float, device) -> float:
+def max_over_ranks(value: float) -> float:
     """Largest `value` over all ranks (the job's wall time is its slowest
-    replica's); identity without an initialised process group."""
+    replica's); identity without an initialised process group.  The reduction
+    runs over the host-side (gloo) group: replicas exchange no device data."""
     import torch
     import torch.distributed as dist
     if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
         return float(value)
-    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    t = torch.tensor([float(value)], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -671,65 +680,48 @@ def whole_job_value(units_per_step: float, steps: int, world: int, elapsed_max: 
     return units_per_step * steps * world / elapsed_max / unit_scale
 
 
+def metric_of(workload: str):
+    """(metric, unit, unit scale) of a workload: GB/s for decode-shaped and
+    KV-cache work, TFLOP/s for prefill-shaped work."""
+    if workload == "kv7b":
+        return "mixed KV-cache quantize+dequantize GB/s, % of roofline", "GB/s", 1e9
+    if is_prefill(workload):
+        return "quantized-linear TOPS (prefill), % of roofline", "TFLOP/s", 1e12
+    return "quantized-linear GB/s (decode M<=256), % of roofline", "GB/s", 1e9
+
+
 # ------------------------------------------------------------------- main
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
-    ap.add_argument("--workload", default="decode7b",
-                    choices=["decode7b", "small", "w8a8-3b", "w8a8-dyn-3b", "prefill", "stack-decode",
-                             "stack-prefill", "stack-fused-decode", "stack-fused-prefill", "kv7b"])
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    a = ap.parse_args()
-    if a.warmup < 3:
-        a.warmup = 3
+def reference_line(a, workload):
+    """The reference arm: the oracle, timed as it stands on the host cores, on a
+    bounded sample of the workload."""
+    metric, metric_unit, unit_scale = metric_of(workload)
+    _, wl = workload_calls(workload)
+    run, units, desc, cores = oracle_sample(workload)
+    for _ in range(a.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        run()
+    dt = (time.perf_counter() - t0) / a.steps
+    v = units / dt / unit_scale
+    return {
+        "impl": "reference", "metric": metric, "value": v, "unit": metric_unit, "n_gpus": 1,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl, "sample": desc},
+        "cpu_baseline": {"value": v, "unit": metric_unit, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": metric_unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    prefill = is_prefill(a.workload)
-    metric_unit = "TFLOP/s" if prefill else "GB/s"
-    metric = ("quantized-linear TOPS (prefill), % of roofline" if prefill
-              else "quantized-linear GB/s (decode M<=256), % of roofline")
-    if a.workload == "kv7b":
-        metric = "mixed KV-cache quantize+dequantize GB/s, % of roofline"
-    lins, wl = workload_calls(a.workload)
-    unit_scale = 1e12 if prefill else 1e9
 
-    if a.impl == "reference":
-        if rank != 0:
-            return
-        run, units, desc, cores = oracle_sample(a.workload)
-        for _ in range(a.warmup):
-            run()
-        t0 = time.perf_counter()
-        for _ in range(a.steps):
-            run()
-        dt = (time.perf_counter() - t0) / a.steps
-        v = units / dt / unit_scale
-        print(json.dumps({
-            "impl": "reference", "metric": metric, "value": v, "unit": metric_unit, "n_gpus": 1,
-            "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl, "sample": desc},
-            "cpu_baseline": {"value": v, "unit": metric_unit, "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": v, "unit": metric_unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
-        return
-
+def measure(a, workload, dev, rank, world, local):
+    """Times `workload` (a.steps steps after a.warmup) and returns its JSON
+    object (on every rank; rank 0 prints it)."""
     import torch
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from bit_quantized_linear_gb300 import capi
+    metric, metric_unit, unit_scale = metric_of(workload)
+    prefill = is_prefill(workload)
 
-    W = KvWorkload(a.workload, dev) if a.workload == "kv7b" else GpuWorkload(a.workload, dev)
+    W = KvWorkload(workload, dev) if workload == "kv7b" else GpuWorkload(workload, dev)
+    wl = W.wl if hasattr(W, "wl") else workload_calls(workload)[1]
     n = len(W.fns)
     units_step = sum(W.call_flops) if prefill else sum(W.call_bytes)
     bytes_step = sum(W.call_bytes)
@@ -768,11 +760,10 @@ def main():
         barrier()
     # graph replays do not pass through the host entry points: count the kernels a step launches
     launches = sum(len(k.split("+")) for k in W.kernel) * a.steps
-    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, dev)
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3)
     clocks = clk.summary()
     ms_step = elapsed / a.steps * 1e3
     value = whole_job_value(units_step, a.steps, world, elapsed, unit_scale)
-
     # ---- timed region 2: per-launch durations (each call bracketed by CUDA events) ----
     dur = np.zeros((a.steps, n))
     if W.events is not None:
@@ -879,7 +870,7 @@ def main():
             W.graphs_e2e[s % W.copies].replay()
         e1.record(W.stream)
         torch.cuda.synchronize()
-        et = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+        et = max_over_ranks(e0.elapsed_time(e1) / 1e3)
         e2e = {"value": whole_job_value(units_step, a.steps, world, et, unit_scale), "unit": metric_unit,
                "h2d_bytes_per_step": int(sum(src.numel() * src.element_size() for _, src in W.h2d)),
                "d2h_bytes_per_step": int(sum(src.numel() * src.element_size() for _, src in W.d2h)),
@@ -889,28 +880,79 @@ def main():
                        "CUDA-graph replay: pinned-host inputs copied in, the step's kernels, outputs copied out")}
 
     stream_ctx.__exit__(None, None, None)
+    dtype, extra_config = W.dtype, W.extra_config
+    del W  # the next workload of the run gets the memory back
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        cpu = cpu_baseline(a.workload, unit_scale, metric_unit)
+        cpu = cpu_baseline(workload, unit_scale, metric_unit)
+    return {
+        "metric": metric, "value": value, "unit": metric_unit, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype,
+        "data": "synthetic",
+        "config": dict({"workload": wl, "bytes_per_step": bytes_step, "flops_per_step": flops_step},
+                       **extra_config,
+                       parallelism=f"replicas{world}" if world > 1 else "single-gpu",
+                       timing="CUDA-graph replay of whole steps, CUDA events around the K steps"),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "calls": calls,
+    }
 
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["qlin", "reference"], default="qlin")
+    ap.add_argument("--workload", default="decode7b",
+                    choices=["decode7b", "small", "w8a8-3b", "w8a8-dyn-3b", "prefill", "stack-decode",
+                             "stack-prefill", "stack-fused-decode", "stack-fused-prefill", "kv7b"])
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="with the default decode workload, skip the E4M3 W8A8 prefill line")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        a.warmup = 3
+    # the default run reports the two halves of the metric: the decode sweep (the
+    # line's own keys) and the prefill workload (its "prefill" object)
+    with_prefill = a.workload == "decode7b" and not a.no_prefill
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        out = reference_line(a, a.workload)
+        if with_prefill:
+            out["prefill"] = reference_line(a, "prefill")
+        print(json.dumps(out))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        # host-side group: the replicas only meet at barriers and one max reduction
+        dist.init_process_group("gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    out = measure(a, a.workload, dev, rank, world, local)
+    if with_prefill:
+        out["prefill"] = measure(a, "prefill", dev, rank, world, local)
     if rank == 0:
-        out = {
-            "metric": metric, "value": value, "unit": metric_unit, "n_gpus": world, "steps": a.steps,
-            "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": W.dtype,
-            "data": "synthetic",
-            "config": dict({"workload": wl, "bytes_per_step": bytes_step, "flops_per_step": flops_step},
-                           **W.extra_config,
-                           parallelism=f"replicas{world}" if world > 1 else "single-gpu",
-                           timing="CUDA-graph replay of whole steps, CUDA events around the K steps"),
-            "roofline": roof,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": int(launches),
-            "clocks": clocks,
-            "calls": calls,
-        }
         print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()

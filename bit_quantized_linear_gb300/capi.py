@@ -33,7 +33,7 @@ EXPORTS = ["qlin_quantize_weight", "qlin_act_scale_from_calib", "qlin_quantize_a
            "qlin_kv_load_mixed", "qlin_w8a16_gate_up_silu", "qlin_w8a8_gate_up_silu"]
 
 # Size of the library-owned scratch of qlin_w8a8_linear_noalloc (QLIN_W8A8_NOALLOC_SCRATCH_BYTES).
-W8A8_NOALLOC_SCRATCH_BYTES = 32 << 20
+W8A8_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class QlinError(RuntimeError):

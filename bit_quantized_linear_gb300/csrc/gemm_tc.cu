@@ -1,30 +1,32 @@
 // Tensor-core (tcgen05) GEMMs for the quantized linear on sm_103a.
 //
-// k_fp8_gemm   W8A8 with E4M3 activations and weights: TMA loads both 8-bit
-//              operand tiles (128-byte swizzle) into a 4-stage shared-memory
-//              ring, one thread issues tcgen05.mma kind::f8f6f4 into a TMEM
-//              accumulator (fp32), four epilogue warps read TMEM and apply
-//              y = acc * (s_x * s_w[n]) + bias[n] -> BF16.
-//              Tile: 128 tokens x BN output channels x 128 k per stage.
+// k_fp8_gemm   W8A8 with E4M3 activations and weights.  Persistent: each CTA
+//              walks 128-token x 256-channel output tiles.  TMA loads both
+//              8-bit operand tiles (128-byte swizzle) into a 4-stage
+//              shared-memory ring, one thread issues tcgen05.mma kind::f8f6f4
+//              into one of two TMEM accumulators (fp32), and eight epilogue
+//              warps read the other accumulator and apply
+//              y = acc * (s_x * s_w[n]) + bias[n] -> BF16 (TMA stores).  The
+//              XQ variant also quantizes the BF16 activations inside the GEMM.
 //
-// k_w8_swap    W8A16 (INT8 or E4M3 weight codes, BF16 activations) with the
-//              weights as the 128-row MMA operand ("swap AB": output channels
-//              on the TMEM lanes, tokens on the MMA N dimension, 16..256), so
-//              decode batches of a few tokens still fill the tensor core's M.
-//              TMA streams raw 8-bit weight tiles and BF16 activation tiles;
-//              four converter warps turn each raw tile into an exact BF16 tile
-//              in the UMMA 128-byte-swizzle layout; one thread issues
-//              tcgen05.mma kind::f16.  When there are too few output tiles to
-//              fill the GPU, the K range is split over the CTAs of a cluster
-//              and the fp32 partial tiles are summed in a fixed order through
-//              distributed shared memory -- one kernel, deterministic, no
-//              global workspace and no spinning on global flags.
+// k_w8_dq      W8A16 (INT8 or E4M3 weight codes, BF16 activations) and the
+//              INT8 W8A8 core, with the weights as the 128-row MMA operand
+//              ("swap AB": output channels on the TMEM lanes, tokens on the
+//              MMA N dimension, 16..256), so decode batches of a few tokens
+//              still fill the tensor core's M.  TMA streams raw 8-bit weight
+//              tiles and BF16 activation tiles; three converter quads turn each
+//              raw tile into exact BF16 and store it into a ring of A operands
+//              in tensor memory (tcgen05.st); two issuer threads alternate
+//              k-blocks of tcgen05.mma kind::f16 (A from TMEM, B from shared
+//              memory).  When there are too few output tiles to fill the GPU,
+//              the K range is split over the CTAs of a cluster and the fp32
+//              partial tiles are summed in a fixed order through distributed
+//              shared memory -- one kernel, deterministic, no global workspace
+//              and no spinning on global flags.
 //
-// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
-// MMA issuer, warps 4..7 = converters (k_w8_swap) and epilogue (TMEM lane
-// quarter = warp % 4).  Every mbarrier wait is bounded (tc::mbar_wait); a wait
-// that runs out sets the device status word and the CTA leaves through the
-// same exit path (TMEM freed, cluster barriers met).
+// Warp roles are listed at each kernel.  Every mbarrier wait is bounded
+// (tc::mbar_wait); a wait that runs out sets the device status word and the CTA
+// leaves through the same exit path (TMEM freed, cluster barriers met).
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
@@ -133,12 +135,6 @@ struct Fp8CfgT {
 };
 using Fp8Cfg = Fp8CfgT<0>;
 
-// MC = 2: the CTAs of a 2-CTA cluster take the two m-tiles of a pair with the
-// same n-tile; each loads its own A tile and half of the shared B tile, which
-// TMA multicasts into both CTAs, so every B byte leaves L2 once per pair.  A
-// stage may be refilled only when both CTAs' MMAs have read it: the MMA
-// commits arrive on the stage's empty barrier in both CTAs.
-//
 // XQ = 1: the activations are quantized inside the kernel.  Warps 2-3 and
 // 12-15 (a 512-thread block) of every CTA take quantization tasks (m-tile,
 // 128-k block).  TMA streams each task's BF16 tile into a ring of 64-row chunks
@@ -152,12 +148,11 @@ using Fp8Cfg = Fp8CfgT<0>;
 // async proxy after either acquire.  The quantization streams from HBM while
 // the GEMM is bound by the tensor cores and L2, so it overlaps.  The launch is
 // cooperative: every CTA is resident, and every wait is bounded besides.
-template <int MC, int XQ>
+template <int XQ>
 __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, Fp8Params p) {
   using C = Fp8CfgT<XQ>;
-  static_assert(MC == 1 || MC == 2, "cluster of one or two CTAs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint64_t *full = (uint64_t *)(smem + C::BAR_OFF);
@@ -167,27 +162,16 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (p.K + C::BK - 1) / C::BK;
-  if constexpr (MC == 2) {
-    // Launched without its 2-CTA cluster shape, the pair's multicasts and peer
-    // barrier arrivals would address a CTA that does not exist: report and leave
-    // before any barrier, TMEM or peer is touched.
-    if (cluster_nctarank() != 2) {
-      if (threadIdx.x == 0) set_status(p.status, QLIN_ERR_UNSUPPORTED);
-      return;
-    }
-  }
-  // work items: tiles (MC = 1) or tile pairs (MC = 2: m-tiles 2q, 2q+1 of one n-tile)
-  const int rank = MC == 2 ? (int)cluster_ctarank() : 0;
-  const int mgroups = (p.mtiles + MC - 1) / MC;
-  const int items = mgroups * p.ntiles, G = gridDim.x / MC, cid = blockIdx.x / MC;
+  // output tiles t = blockIdx.x + j * gridDim.x, m-tile major
+  const int items = p.mtiles * p.ntiles, G = gridDim.x, cid = blockIdx.x;
   const int my_tiles = (cid < items) ? (items - cid + G - 1) / G : 0;
-  auto tile_m0 = [&](int t) { return ((t / p.ntiles) * MC + rank) * C::BM; };
+  auto tile_m0 = [&](int t) { return (t / p.ntiles) * C::BM; };
   auto tile_n0 = [&](int t) { return (t % p.ntiles) * C::BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC);  // the MMA commits of every CTA that reads the stage's B tile
+      mbar_init(&empty[s], 1);  // the MMA commit that has read the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -213,7 +197,6 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (MC == 2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
   pdl_trigger();
@@ -231,7 +214,7 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
       for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
         const int t = cid + j * G;
         const int m0 = tile_m0(t), n0 = tile_n0(t);
-        bool tile_ready = true;  // also for the empty second m-tile of a pair past M (no codes)
+        bool tile_ready = true;
         if constexpr (XQ == 1) {
           const int band = (m0 / C::BM) / p.xq_band;
           if (m0 < p.M && band > ready_band) {
@@ -282,17 +265,11 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
           tma_load_2d(&tm_a, &full[s], st, kb * C::BK, m0);
           // B: two boxes of 128 rows; glu: the gate rows n0/2.. and the matching up rows N + n0/2..
           const int b0 = p.glu ? n0 / 2 : n0, b1 = p.glu ? p.N + n0 / 2 : n0 + C::BN / 2;
-          if constexpr (MC == 2) {  // this CTA loads box `rank` for both CTAs of the pair
-            tma_load_2d_mc(&tm_b, &full[s], st + C::A_BYTES + rank * (C::B_BYTES / 2), kb * C::BK,
-                           rank ? b1 : b0, (uint16_t)0x3);
-          } else {
-            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, b0);
-            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, b1);
-          }
+          tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, b0);
+          tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, b1);
         }
       }
-      // abort: the stages this CTA armed land before it leaves (with a pair, a
-      // stage whose peer half never comes gives up after the drain limit)
+      // abort: the stages this CTA armed land before it leaves
       if (*abort_flag) drain_ring(full, C::STAGES, i, C::STAGES);
     }
   } else if (XQ == 1 && (warp == 2 || warp == 3 || warp >= 12)) {  // ----- activation quantizer
@@ -445,8 +422,7 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
           mma_fp8(dt, ad + 2, bd + 2, C::IDESC, 1u);
           mma_fp8(dt, ad + 4, bd + 4, C::IDESC, 1u);
           mma_fp8(dt, ad + 6, bd + 6, C::IDESC, 1u);
-          if constexpr (MC == 2) mma_commit_mc(&empty[s], (uint16_t)0x3);
-          else mma_commit(&empty[s]);
+          mma_commit(&empty[s]);
         }
         if (!ok) break;
         mma_commit(&acc_full[b]);
@@ -604,13 +580,6 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // neither CTA of a pair leaves while the other may still multicast into it or
-  // arrive on its barriers (every wait above is bounded, so both get here); on
-  // the abort path what the peer sent before the barrier is given time to land
-  if constexpr (MC == 2) {
-    cluster_sync();
-    if (*abort_flag) peer_grace();
-  }
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -1322,12 +1291,7 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   Fp8Params p{(int)g.M, (int)g.N, (int)g.K, mtiles, ntiles, g.x_scale_per_token, g.glu,
               (uint8_t *)g.a, g.xq_flags, (nkb + 3) / 4 * 4, 1, g.w_scale, g.x_scale,
               g.bias, (uint16_t *)g.y, dev.status};
-  // band of quantization tasks: the m-tiles one wave of `slots` work items spans
-  auto band = [&](int slots, int mc) {
-    const int b = mc * ((slots + ntiles - 1) / ntiles);
-    return b < mtiles ? b : mtiles;
-  };
-  if (g.xq) {  // fused quantization: cooperative launch; pairs share B where clusters combine with it
+  if (g.xq) {  // fused quantization: cooperative launch (every CTA resident)
     if (g.x_scale_per_token || !g.xq_flags) return cudaErrorInvalidValue;
     CUtensorMap tx;  // the BF16 activations, chunks of XQ_ROWS rows of a 128 x 128 task tile
     if (!make_map(&tx, g.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, Fp8CfgT<1>::XQ_ROWS,
@@ -1337,35 +1301,19 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
     cudaError_t e = cudaMemsetAsync(g.xq_flags, 0, fb, st);
     if (e != cudaSuccess) return e;
     using CX = Fp8CfgT<1>;
-    static cudaError_t a2 = set_smem(k_fp8_gemm<2, 1>, CX::SMEM);
-    static cudaError_t a1 = set_smem(k_fp8_gemm<1, 1>, CX::SMEM);
-    static bool pairs_ok = true;  // cleared if this device refuses cooperative cluster launches
-    if (mtiles >= 2 && pairs_ok && a2 == cudaSuccess) {
-      const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
-      const int grid = 2 * (items < pairs ? items : pairs);
-      p.xq_band = band(grid / 2, 2);
-      e = launch_kernel_coop(k_fp8_gemm<2, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 2, ta, tb,
-                             tx, ty, p);
-      if (e == cudaSuccess) return e;
-      pairs_ok = false;
-    }
+    static cudaError_t a1 = set_smem(k_fp8_gemm<1>, CX::SMEM);
     if (a1 != cudaSuccess) return a1;
     const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-    p.xq_band = band(grid, 1);
-    return launch_kernel_coop(k_fp8_gemm<1, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 1, ta, tb,
-                              tx, ty, p);
+    // band of quantization tasks: the m-tiles one wave of `grid` tiles spans
+    const int b = (grid + ntiles - 1) / ntiles;
+    p.xq_band = b < mtiles ? b : mtiles;
+    return launch_kernel_coop(k_fp8_gemm<1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 1, ta, tb, tx,
+                              ty, p);
   }
-  if (mtiles >= 2) {  // pairs of m-tiles share their B tiles (2-CTA clusters, TMA multicast)
-    static cudaError_t attr2 = set_smem(k_fp8_gemm<2, 0>, C::SMEM);
-    if (attr2 != cudaSuccess) return attr2;
-    const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
-    const int grid = 2 * (items < pairs ? items : pairs);
-    return launch_kernel_x(k_fp8_gemm<2, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 2, ta, tb, tb, ty, p);
-  }
-  static cudaError_t attr = set_smem(k_fp8_gemm<1, 0>, C::SMEM);
+  static cudaError_t attr = set_smem(k_fp8_gemm<0>, C::SMEM);
   if (attr != cudaSuccess) return attr;
   const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-  return launch_kernel(k_fp8_gemm<1, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, ty, p);
+  return launch_kernel(k_fp8_gemm<0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, ty, p);
 }
 
 // Token tile (MMA N) of the W8A16 swap-AB kernel.  Up to 128 tokens the tile
@@ -1389,11 +1337,10 @@ size_t fp8_xq_flag_bytes(int64_t M, int64_t K) {
 // tile's main loop is long and the quantization a large share of the work:
 // K >= 4096, at most 4096 GEMM columns, and 64 m-tiles or more (8192 tokens);
 // at K = 2048 the separate pass with the TMA-store epilogue is 20-28% faster.
-// Its quantizers are the GEMM's CTAs, so the tile pairs must fill every SM.
+// Its quantizers are the GEMM's CTAs, so the output tiles must fill every SM.
 // N counts GEMM columns (2I for the merged gate_up).
 // QLIN_FP8_FUSED_QUANT=0 in the environment (read once) keeps the separate
-// quantization pass everywhere: a profiler that re-issues cooperative launches
-// without their cluster shape cannot run the fused kernel.
+// quantization pass everywhere, so the two forms can be compared on one shape.
 bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms) {
   static const bool enabled = [] {
     const char *v = std::getenv("QLIN_FP8_FUSED_QUANT");
@@ -1401,7 +1348,7 @@ bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms) {
   }();
   if (!enabled) return false;
   const int64_t mtiles = (M + Fp8Cfg::BM - 1) / Fp8Cfg::BM, ntiles = (N + Fp8Cfg::BN - 1) / Fp8Cfg::BN;
-  return mtiles >= 64 && K >= 4096 && N <= 4096 && ((mtiles + 1) / 2) * ntiles >= sms / 2;
+  return mtiles >= 64 && K >= 4096 && N <= 4096 && mtiles * ntiles >= sms;
 }
 
 int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms) {

@@ -5,6 +5,8 @@
 
 #include <utility>
 
+#include "qlin.h"
+
 namespace qlin {
 
 struct DeviceInfo {
@@ -16,6 +18,12 @@ struct DeviceInfo {
 
 // Host-side count of kernels enqueued by the library (qlin_launch_count).
 void note_launches(int n);
+
+// Argument checks of the W8A8 static linear apart from its workspace, and the
+// current-device check (qlin_api.cu); QLIN_OK or the status to return.
+qlin_status w8a8_check_args(int qtype, int64_t M, int64_t K, int64_t N, const void *x, const float *input_scale,
+                            const void *qw, const float *w_scale, const void *bias, const void *y);
+qlin_status device_ready();
 
 // Launches `kernel` on `st` with programmatic stream serialization (the kernel
 // calls pdl_wait() before reading global inputs) and an optional cluster
@@ -159,8 +167,6 @@ struct KvArgs {
 cudaError_t launch_kv_store(const KvArgs &a, unsigned *status, int sms, cudaStream_t st);
 cudaError_t launch_kv_load(const KvArgs &a, unsigned *status, cudaStream_t st);
 
-cudaError_t launch_gemm_simt(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
-
 // tcgen05 kernels (gemm_tc.cu)
 cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
 cudaError_t launch_w8a16_swap(const GemmArgs &g, const DeviceInfo &dev, cudaStream_t st);
@@ -177,8 +183,5 @@ cudaError_t launch_i8_to_bf16(int64_t M, int64_t K, const void *q, void *out, in
 // Dynamic per-token quantization: scales s[M]; codes (1 byte) or INT8 codes as BF16.
 cudaError_t launch_quantize_act_dyn(int qtype, bool out_bf16, int64_t M, int64_t K, const void *x, float *s, void *q,
                                     cudaStream_t st);
-
-cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
-                              cudaStream_t st);
 
 }  // namespace qlin

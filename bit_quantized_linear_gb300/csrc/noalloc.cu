@@ -10,8 +10,9 @@ namespace qlin {
 
 // Scratch of the allocation-free W8A8 entry point.  A file-scope device array:
 // every GPU that loads the library holds it until the process exits.  All calls
-// on a device share it; nothing in it has to start at zero (each call writes
-// the whole region it reads).
+// on a device share it.  A call reads only what it wrote itself: the codes it
+// quantized, and the fused FP8 GEMM's task flags, which the call clears on its
+// stream before the GEMM starts.
 static __device__ __align__(256) uint8_t g_w8a8_scratch[QLIN_W8A8_NOALLOC_SCRATCH_BYTES];
 
 // Host code cannot pass the array's name to a kernel (on the host it is only a
@@ -40,9 +41,12 @@ extern "C" qlin_status qlin_w8a8_linear_noalloc(qlin_qtype qtype, int64_t M, int
                                                 const void *x, const float *input_scale, const void *qw,
                                                 const float *w_scale, const void *bias, void *y,
                                                 qlin_stream_t stream) {
-  const size_t need = qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N);
-  if (need == (size_t)-1) return QLIN_ERR_INVALID_ARG;
-  if (need > QLIN_W8A8_NOALLOC_SCRATCH_BYTES) return QLIN_ERR_WORKSPACE;
+  // the checks of qlin_w8a8_linear in its order: arguments, size, device
+  if (qlin_status s = qlin::w8a8_check_args(qtype, M, K, N, x, input_scale, qw, w_scale, bias, y)) return s;
+  if (qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N) > QLIN_W8A8_NOALLOC_SCRATCH_BYTES)
+    return QLIN_ERR_WORKSPACE;
+  if (qlin_status s = qlin::device_ready()) return s;
+  if (M == 0) return QLIN_OK;
   void *scratch = nullptr;
   if (qlin_status s = qlin::scratch_address(&scratch)) return s;
   return qlin_w8a8_linear(qtype, M, K, N, x, input_scale, qw, w_scale, bias, y, scratch,

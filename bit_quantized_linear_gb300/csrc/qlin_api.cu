@@ -54,6 +54,25 @@ static qlin_status current_device(DeviceInfo **out) {
   return QLIN_OK;
 }
 
+// Failure-detection check kernel: waits on a flag with a global-time limit.
+__global__ void k_debug_wait(const volatile uint32_t *flag, uint64_t timeout_ns, unsigned *status) {
+  pdl_wait();
+  pdl_trigger();
+  const uint64_t t0 = globaltimer_ns();
+  while (*flag == 0u) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      set_status(status, QLIN_ERR_TIMEOUT);
+      return;
+    }
+    __nanosleep(1000);
+  }
+}
+
+cudaError_t launch_debug_wait(const uint32_t *flag, uint64_t timeout_ns, unsigned *status,
+                              cudaStream_t st) {
+  return launch_kernel(k_debug_wait, dim3(1), dim3(1), 0, st, 1, (const volatile uint32_t *)flag, timeout_ns, status);
+}
+
 static inline bool al16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static inline bool valid_qtype(int t) { return t == QLIN_INT8 || t == QLIN_E4M3; }
 static inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -77,6 +96,25 @@ static bool i8_fused_quant(int64_t M) { return M <= 64; }
 static qlin_status check_glu_shape(int64_t M, int64_t K, int64_t I) {
   if (I < 128 || (I % 128) || I > (int64_t)1 << 30) return QLIN_ERR_INVALID_ARG;
   return check_linear_shape(M, K, 2 * I);
+}
+
+// Argument checks of the W8A8 static linear, apart from its workspace (the
+// allocation-free entry point makes the same checks in the same order).
+qlin_status w8a8_check_args(int qtype, int64_t M, int64_t K, int64_t N, const void *x, const float *input_scale,
+                            const void *qw, const float *w_scale, const void *bias, const void *y) {
+  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = check_linear_shape(M, K, N)) return s;
+  if (!input_scale || !qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias)) ||
+      ((uintptr_t)input_scale & 3u))
+    return QLIN_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
+  return QLIN_OK;
+}
+
+// QLIN_OK when the current device is one the library runs on (sm_103a).
+qlin_status device_ready() {
+  DeviceInfo *dev;
+  return current_device(&dev);
 }
 
 }  // namespace qlin
@@ -252,12 +290,7 @@ qlin_status qlin_w8a8_linear(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, 
                              const float *input_scale, const void *qw, const float *w_scale,
                              const void *bias, void *y, void *ws, size_t ws_bytes,
                              qlin_stream_t stream) {
-  if (!valid_qtype(qtype)) return QLIN_ERR_INVALID_ARG;
-  if (qlin_status s = check_linear_shape(M, K, N)) return s;
-  if (!input_scale || !qw || !w_scale || !al16(qw) || !al16(w_scale) || (bias && !al16(bias)) ||
-      ((uintptr_t)input_scale & 3u))
-    return QLIN_ERR_INVALID_ARG;
-  if (M > 0 && (!x || !y || !al16(x) || !al16(y))) return QLIN_ERR_INVALID_ARG;
+  if (qlin_status s = w8a8_check_args(qtype, M, K, N, x, input_scale, qw, w_scale, bias, y)) return s;
   const size_t need = qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype, M, K, N);
   if (need && (!ws || !al16(ws) || ws_bytes < need)) return QLIN_ERR_WORKSPACE;
   DeviceInfo *dev;

@@ -63,7 +63,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // CTA issued to land before it leaves: no async write may reach shared memory
 // the next CTA on the SM already owns.  A copy in flight lands within
 // microseconds; the limit only ends waits for phases that can no longer
-// complete (a peer that stopped before sending its half).
+// complete.
 constexpr uint64_t kDrainLimitNs = 20000000ull;  // 20 ms
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
   const uint32_t addr = smem_u32(bar);
@@ -78,14 +78,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) 
 __device__ __forceinline__ void drain_ring(uint64_t *bars, int stages, int issued, int window) {
   for (int k = issued > window ? issued - window : 0; k < issued; ++k)
     mbar_wait_drain(&bars[k % stages], (uint32_t)(k / stages) & 1);
-}
-// After a cluster's CTAs have all stopped issuing (past a cluster barrier), the
-// copies and commit arrivals a peer sent towards this CTA before that barrier
-// are given time to land before the CTA leaves (abort path only).
-constexpr uint64_t kPeerGraceNs = 1000000ull;  // 1 ms
-__device__ __forceinline__ void peer_grace() {
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < kPeerGraceNs) __nanosleep(1000);
 }
 
 // Named barrier `id` over `nthreads` threads (a multiple of 32) that also ANDs
@@ -313,38 +305,12 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 // Arrives on `bar` once every tcgen05.mma issued so far by this thread completes.
-// TMA 2D load multicast to the CTAs of the cluster in `cta_mask`: the tile lands
-// at the same shared-memory offset in each, and each one's mbarrier at `bar`'s
-// offset receives the complete_tx bytes.
-__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap *tm, uint64_t *bar, void *dst, int c0, int c1,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
-
-// tcgen05.commit arriving on the mbarrier at `bar`'s offset in every CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
 
 // ------------------------------------------------------------------ cluster
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 // CTAs in this CTA's cluster (1 for a launch without a cluster shape).
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;

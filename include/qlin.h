@@ -222,23 +222,30 @@ qlin_status qlin_i8_gemm_s32(int64_t M, int64_t K, int64_t N, const void *qx, co
  * available or not allowed: inference plugins handed a fixed memory budget,
  * code enqueued while a stream is being captured into a CUDA graph, or
  * runtimes that must not grow device memory after start-up.  It computes
- * exactly what qlin_w8a8_linear computes, with the same arguments minus the
- * workspace: the quantized activations go to a scratch array that the library
- * holds in device memory of its own (a file-scope __device__ array of
- * QLIN_W8A8_NOALLOC_SCRATCH_BYTES bytes, 32 MiB, which every GPU that loads the
- * library keeps until the process exits).
+ * exactly what qlin_w8a8_linear computes (the same kernels on the same
+ * inputs, so the same bits), with the same arguments minus the workspace: the
+ * quantized activations (and, for large E4M3 calls, the task flags of the
+ * fused-quantization GEMM) go to a scratch array that the library holds in
+ * device memory of its own (a file-scope __device__ array of
+ * QLIN_W8A8_NOALLOC_SCRATCH_BYTES bytes, 64 MiB, which every GPU that loads
+ * the library keeps until the process exits).
+ *   - Argument errors are reported exactly as qlin_w8a8_linear reports them,
+ *     from the same checks in the same order: arguments, then size, then the
+ *     device (QLIN_ERR_UNSUPPORTED on a GPU other than sm_103a).
  *   - Sizes whose workspace (qlin_workspace_bytes(QLIN_OP_W8A8_LINEAR, qtype,
  *     M, K, N)) exceeds QLIN_W8A8_NOALLOC_SCRATCH_BYTES are rejected with
  *     QLIN_ERR_WORKSPACE before anything is launched.
- *   - The first call on a device looks up the scratch array's device address
- *     (once per device, with that device current); make that first call before
- *     any stream capture begins.
- *   - Every call on a device shares the one scratch array, and each call
- *     overwrites what the previous call left there.  Calls that can overlap on
- *     the GPU (different streams without ordering) race on it; order them.
+ *   - The first call with M > 0 on a device looks up the scratch array's
+ *     device address (once per device, with that device current); make that
+ *     first call before any stream capture begins.
+ *   - Every call on a device shares the one scratch array, which keeps what the
+ *     last call left there.  A call reads only what it has written itself; the
+ *     task flags that must start at zero are cleared by the call, on its
+ *     stream, before its GEMM runs.  Calls that can overlap on the GPU
+ *     (different streams without ordering) race on the array; order them.
  * It calls no cudaMalloc, cudaFree or allocating library routine.
  */
-#define QLIN_W8A8_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+#define QLIN_W8A8_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 qlin_status qlin_w8a8_linear_noalloc(qlin_qtype qtype, int64_t M, int64_t K, int64_t N, const void *x,
                                      const float *input_scale, const void *qw, const float *w_scale,
                                      const void *bias, void *y, qlin_stream_t stream);

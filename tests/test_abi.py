@@ -118,7 +118,7 @@ def test_invalid_arguments_rejected_on_host(capi):
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 4096, 4112) == "k_quantize_act+k_fp8_gemm"
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 2048, 2048) == "k_quantize_act+k_fp8_gemm"
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8064, 11008, 2048) == "k_quantize_act+k_fp8_gemm"
-    # one n-tile: the pairs would not fill the SMs
+    # one n-tile: the tiles would not fill the SMs
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 8192, 11008, 256) == "k_quantize_act+k_fp8_gemm"
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, 1, 1024, 2048, 11008) == "k_quantize_act+k_fp8_gemm"
 
@@ -152,3 +152,43 @@ def test_fused_quant_switch_selects_the_separate_pass():
     out = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True, text=True,
                          timeout=300)
     assert out.stdout.split() == ["k_fp8_gemm<xq>"] * 2
+
+
+def test_noalloc_reports_as_the_workspace_entry_point(capi):
+    """qlin_w8a8_linear_noalloc makes qlin_w8a8_linear's checks in the same
+    order (arguments, size, device), so both return the same status for the
+    same bad call.  Calls that pass every argument check reach the device check
+    only where no device is present (they would launch on fake pointers)."""
+    import torch
+    L = capi.lib()
+    P = ctypes.c_void_p
+    good, odd = P(4096), P(4096 + 8)
+    big_ws = 1 << 40  # never dereferenced: every call below stops before a launch
+
+    def both(qt, M, K, N, x, sx, qw, s, b, y):
+        ws = L.qlin_w8a8_linear(qt, M, K, N, x, sx, qw, s, b, y, good, big_ws, None)
+        na = L.qlin_w8a8_linear_noalloc(qt, M, K, N, x, sx, qw, s, b, y, None)
+        return ws, na
+
+    INV = capi.QLIN_ERR_INVALID_ARG
+    bad = [(9, 4, 64, 64, good, good, good, good, None, good),     # unknown qtype
+           (0, 4, 72, 64, good, good, good, good, None, good),     # K not a multiple of 16
+           (1, 4, 64, 40, good, good, good, good, None, good),     # N not a multiple of 16
+           (1, -1, 64, 64, good, good, good, good, None, good),    # negative M
+           (0, 4, 64, 64, None, good, good, good, None, good),     # no x
+           (1, 4, 64, 64, good, None, good, good, None, good),     # no input_scale
+           (1, 4, 64, 64, good, P(4098), good, good, None, good),  # input_scale not 4-byte aligned
+           (0, 4, 64, 64, good, good, odd, good, None, good),      # qw misaligned
+           (1, 4, 64, 64, good, good, good, good, odd, good),      # bias misaligned
+           (0, 4, 64, 64, good, good, good, good, None, odd)]      # y misaligned
+    for args in bad:
+        assert both(*args) == (INV, INV), args
+    # beyond the scratch: the size check answers before the device check
+    assert L.qlin_w8a8_linear_noalloc(1, 65536, 2048, 64, good, good, good, good, None, good, None) == \
+        capi.QLIN_ERR_WORKSPACE
+    assert L.qlin_w8a8_linear(1, 65536, 2048, 64, good, good, good, good, None, good, good, 64 << 20, None) == \
+        capi.QLIN_ERR_WORKSPACE
+    if not torch.cuda.is_available():
+        for args in [(1, 0, 64, 64, None, good, good, good, None, None), (0, 4, 64, 64, good, good, good, good, None, good)]:
+            ws, na = both(*args)
+            assert ws == na and ws in (capi.QLIN_ERR_UNSUPPORTED, capi.QLIN_ERR_CUDA), (args, ws, na)

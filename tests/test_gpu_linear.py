@@ -300,15 +300,16 @@ def test_bounded_wait_reports_timeout(capi):
 @pytest.mark.parametrize("qt", ["int8", "e4m3"])
 @pytest.mark.parametrize("M,K,N", [(64, 1040, 1024), (100, 2048, 1024), (200, 1040, 2048), (256, 3584, 4096),
                                    (700, 2048, 2048), (1024, 1024, 4096)])
-def test_w8a16_activation_multicast_shapes(capi, qt, M, K, N):
-    """Shapes whose channel tiles group in twos / fours, so clusters share (multicast)
-    activation tiles; ragged M and K included."""
+def test_w8a16_split_k_cluster_shapes(capi, qt, M, K, N):
+    """Shapes with few output tiles, whose K range is split over the CTAs of a
+    cluster (the partial tiles are summed through distributed shared memory),
+    and shapes past the 128-token tile; ragged M and K included."""
     rows = None if M <= 256 else sample_rows(M, 24)
-    w8a16_case(capi, qt, M, K, N, True, "mcast", rows=rows, outliers=True)
+    w8a16_case(capi, qt, M, K, N, True, "splitk", rows=rows, outliers=True)
 
 
 @pytest.mark.parametrize("M,K,N", [(64, 1040, 1024), (200, 2048, 2048)])
-def test_i8_gemm_multicast_bitexact(capi, M, K, N):
+def test_i8_gemm_split_k_bitexact(capi, M, K, N):
     rng = np.random.default_rng(M + K + N)
     qx = rng.integers(-127, 128, (M, K), dtype=np.int8)
     qw = rng.integers(-127, 128, (N, K), dtype=np.int8)

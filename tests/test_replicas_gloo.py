@@ -21,7 +21,7 @@ def _worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     elapsed = [0.75, 1.25][rank]
-    m = bench.max_over_ranks(elapsed, "cpu")
+    m = bench.max_over_ranks(elapsed)
     v = bench.whole_job_value(units_per_step=1e9, steps=10, world=world, elapsed_max=m, unit_scale=1e9)
     dist.barrier()
     out[rank] = (m, v)
@@ -42,5 +42,5 @@ def test_two_replicas_agree_on_slowest_and_sum_units():
 
 def test_single_process_is_identity():
     import bench
-    assert bench.max_over_ranks(0.5, "cpu") == 0.5
+    assert bench.max_over_ranks(0.5) == 0.5
     assert bench.whole_job_value(2e9, 4, 1, 2.0, 1e9) == pytest.approx(4.0)
