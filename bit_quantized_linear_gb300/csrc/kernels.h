@@ -140,7 +140,7 @@ struct GemmArgs {
 };
 
 // E4M3 W8A16 on the FP8 tensor cores (w8a16_f8.cu): up to kW8A16F8MaxM tokens,
-// plain or merged gate_up; the activations are split into two E4M3 terms in
+// plain or merged gate_up; the activations are split into four E4M3 terms in
 // the workspace (w8a16_f8_workspace bytes).
 constexpr int kW8A16F8MaxM = 32;
 int w8a16_f8_tt(int64_t M);

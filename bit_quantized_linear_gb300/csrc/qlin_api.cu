@@ -211,7 +211,7 @@ size_t qlin_workspace_bytes(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K, 
     case QLIN_OP_QUANTIZE_WEIGHT: return 0;
     case QLIN_OP_ACT_SCALE: return 256;
     case QLIN_OP_QUANTIZE_ACT: return 0;
-    // E4M3 up to kW8A16F8MaxM tokens: the activations' two E4M3 terms and per-token scales
+    // E4M3 up to kW8A16F8MaxM tokens: the activations' four E4M3 terms and per-token scales
     case QLIN_OP_W8A16_LINEAR:
     case QLIN_OP_W8A16_GATE_UP_SILU:
       return (qtype == QLIN_E4M3 && M > 0 && M <= kW8A16F8MaxM) ? w8a16_f8_workspace(M, K) : 0;

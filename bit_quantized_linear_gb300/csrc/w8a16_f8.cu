@@ -5,20 +5,32 @@
 //
 // The weight stream is the cost of a small-batch linear, and turning every code
 // into BF16 before a BF16 MMA costs more issue slots than the stream leaves.
-// Instead the activations, which are few, are put into the weights' format:
-// each token row x_m gets a power-of-two scale s_m (the least with
-// 448 s_m >= max |x_m|), and x_m / s_m is split into two E4M3 terms
-//     x1 = RN_e4m3(x / s),  x2 = RN_e4m3(16 (x / s - x1)),  x / s = x1 + x2 / 16.
-// For |x / s| >= 2^-6 the split is exact: x1 keeps the leading 4 significant
-// bits, the remainder is a multiple of 2^(e-7) below 2^(e-3) (e the exponent of
-// x / s), so 16 times it has at most 4 significant bits from 2^(e-3) >= 2^-9
-// upwards, which E4M3 holds.  Smaller elements (|x| below about 2^-13.8 of the
-// row's maximum) are kept to an absolute error of 2^-14 s.  Then
-//     sum_k w[n,k] x[m,k] = s_m (sum_k w x1 + (1/16) sum_k w x2),
-// two FP8 products read straight from the weight codes: one E4M3 MMA with the
-// two terms of every token as 2 x BNT columns of the B operand (swap AB: the
+// Instead the activations, which are few, are put into the weights' format.
+// Each token row x_m gets a power-of-two scale s_m (the least with
+// 448 s_m >= max |x_m|), and every element v = x / s_m is written as two E4M3
+// terms in one of two bands:
+//   band A, |v| >= 2^-6:  x1 = RN_e4m3(v),  x2 = RN_e4m3(16 (v - x1)),
+//                         v = x1 + x2 / 16;
+//   band B, |v| <  2^-6:  with v' = 2^14 v,
+//                         x3 = RN_e4m3(v'), x4 = RN_e4m3(16 (v' - x3)),
+//                         v = 2^-14 (x3 + x4 / 16);
+// the terms of the other band are zero.  A band's split is exact whenever its
+// value (v, or v') is at least 2^-6 in magnitude: the first term keeps the
+// leading 4 significant bits, the remainder is a multiple of 2^(e-7) below
+// 2^(e-3) (e the exponent of the value, e >= -6), so 16 times it has at most 4
+// significant bits from 2^(e-3) >= 2^-9 upwards, which E4M3 holds (the
+// subnormals reach down to 2^-9; a BF16 value has 8 significant bits).  So
+// every element with |x| >= 2^-20 s_m, which includes everything within
+// 2^-28.8 of the row's maximum, is represented exactly; the rest keep an
+// absolute error of at most 2^-28 s_m (below 2^-35.8 of the row's maximum).
+// A row whose few "massive" channels dwarf the others by 2^20 therefore still
+// has its ordinary elements exact.  Then
+//   sum_k w[n,k] x[m,k] = s_m (A1 + A2 / 16 + 2^-14 (A3 + A4 / 16)),
+//   Aj = sum_k w[n,k] xj[m,k],
+// four FP8 products read straight from the weight codes: one E4M3 MMA with the
+// four terms of every token as 4 x TT columns of the B operand (swap AB: the
 // weight rows are the MMA's 128 rows, so one token still fills the tensor
-// core's M), and an epilogue that forms s_m s_w[n] (acc1 + acc2 / 16) + b[n].
+// core's M), and an epilogue that forms s_m s_w[n] (...) + b[n].
 // INT8 weights: the same with the INT8 codes read as E4M3 would be wrong, so
 // this path is E4M3 only.
 #include <cuda.h>
@@ -42,10 +54,11 @@ namespace {
 // Token row m, chunk c of kSplitChunk elements: one CTA.  Every CTA of a row
 // reads the whole row for its abs-max (the row is small and L2-resident; all of
 // a thread's loads are issued before any is used) and keeps its own chunk in
-// registers, then writes that chunk's two E4M3 terms into the B-operand
-// layout: token tile j (tt tokens) owns rows [2 tt j, 2 tt j + 2 tt) of xs, x1
-// of its tokens first, then x2.
+// registers, then writes that chunk's four E4M3 terms into the B-operand
+// layout: token tile j (tt tokens) owns rows [4 tt j, 4 tt j + 4 tt) of xs,
+// the x1 rows of its tokens first, then x2, x3 and x4.
 constexpr int kSplitThreads = 256, kSplitChunk = 8 * kSplitThreads, kSplitMaxLoads = 16;
+constexpr int kSplitTerms = 4;  // x1, x2 (band A) and x3, x4 (band B)
 
 // Least power of two s with 448 s >= a (a > 0), from the exponent bits alone:
 // a = f 2^e with f in [1, 2); 448 = 1.75 2^8, so s = 2^(e-8) when f <= 1.75,
@@ -106,22 +119,35 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
   if (blockIdx.x == 0 && threadIdx.x == 0) xscale[m] = s;
   if (mine >= n8) return;
   const int j = m / tt, t = m % tt;
-  uint8_t *x1 = xs + ((size_t)2 * tt * j + t) * K, *x2 = x1 + (size_t)tt * K;
+  uint8_t *x1 = xs + ((size_t)kSplitTerms * tt * j + t) * K;
+  const size_t term = (size_t)tt * K;  // x2, x3, x4 follow, tt rows apart
   const uint32_t w[4] = {own.x, own.y, own.z, own.w};
-  uint32_t h[4], l[4];  // codes of x1 and x2, two per 16 bits
+  uint32_t c[kSplitTerms][4];  // codes of x1..x4, two per 16 bits
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float v0 = bf16_bits_to_f32(w[e] & 0xFFFFu) * r, v1 = bf16_bits_to_f32(w[e] >> 16) * r;
-    const __nv_fp8x2_storage_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
-    const float2 f1 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3)));
-    // the remainders are exact in fp32; times 16 they fit E4M3 (see above)
-    const __nv_fp8x2_storage_t c2 =
-        __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v0 - f1.x), 16.0f * (v1 - f1.y)), __NV_SATFINITE, __NV_E4M3);
-    h[e] = c1;
-    l[e] = c2;
+    float v[2] = {bf16_bits_to_f32(w[e] & 0xFFFFu) * r, bf16_bits_to_f32(w[e] >> 16) * r};  // exact
+    // band B: the element scaled by 2^14 (exact), split the same way into x3, x4
+    bool lo[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      lo[h] = fabsf(v[h]) < 0.015625f;  // |v| < 2^-6
+      if (lo[h]) v[h] *= 16384.0f;
+    }
+    const __nv_fp8x2_storage_t h1 = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
+    const float2 f1 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h1, __NV_E4M3)));
+    // the remainders are exact in fp32; times 16 they fit E4M3 (see the file's head)
+    const __nv_fp8x2_storage_t h2 =
+        __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v[0] - f1.x), 16.0f * (v[1] - f1.y)), __NV_SATFINITE, __NV_E4M3);
+    // each element's two codes go to its band's pair of terms, zero to the other pair
+    const uint32_t m0 = lo[0] ? 0x0000u : 0x00FFu, m1 = lo[1] ? 0x0000u : 0xFF00u;
+    const uint32_t a1 = (uint32_t)h1 & (m0 | m1), a2 = (uint32_t)h2 & (m0 | m1);
+    const uint32_t b1 = (uint32_t)h1 & (~(m0 | m1) & 0xFFFFu), b2 = (uint32_t)h2 & (~(m0 | m1) & 0xFFFFu);
+    c[0][e] = a1, c[1][e] = a2, c[2][e] = b1, c[3][e] = b2;
   }
-  *reinterpret_cast<uint2 *>(x1 + 8 * mine) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-  *reinterpret_cast<uint2 *>(x2 + 8 * mine) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+#pragma unroll
+  for (int q = 0; q < kSplitTerms; ++q)
+    *reinterpret_cast<uint2 *>(x1 + q * term + 8 * mine) =
+        make_uint2(c[q][0] | (c[q][1] << 16), c[q][2] | (c[q][3] << 16));
 }
 
 // ------------------------------------------------------------ the FP8 linear
@@ -132,16 +158,16 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
 // leaves its fp32 partial tile in shared memory (the drained ring) and the
 // cluster sums them in rank order through distributed shared memory, each CTA
 // finishing a slice of the outputs.
-template <int TT>  // token tile; the MMA's N is 2 TT (both terms of each token)
+template <int TT>  // token tile; the MMA's N is 4 TT (the four terms of each token)
 struct W8F8Cfg {
-  static constexpr int BM = 128, BK = 128, NB = 2 * TT;
+  static constexpr int BM = 128, BK = 128, NB = kSplitTerms * TT;
   static constexpr int A_BYTES = BM * BK, B_BYTES = NB * BK, STAGE = A_BYTES + B_BYTES;
   // The ring depth is a launch parameter (stages of STAGE bytes; the barriers
   // follow the ring).
   static constexpr int MAX_STAGES = 14, BAR_BYTES = 256;
   static constexpr int PART_BYTES = TT * BM * 4;  // [TT tokens][BM rows] fp32, in the drained ring
   static constexpr int THREADS = 192;
-  static constexpr uint32_t TMEM_COLS = NB;  // 32 or 64, a power of two
+  static constexpr uint32_t TMEM_COLS = NB;  // 64 or 128, a power of two
   static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, NB);
   static constexpr int smem_bytes(int stages) { return stages * STAGE + BAR_BYTES + 1024; }
   static_assert(PART_BYTES <= 2 * STAGE, "partial tile in a ring of two or more stages");
@@ -284,13 +310,18 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
       float *part = reinterpret_cast<float *>(smem);   // the ring is drained: every MMA has read it
 #pragma unroll 1
       for (int c = 0; c < TT; c += 16) {
-        uint32_t a1[16], a2[16];  // x1 and x2 products of tokens c..c+15
+        uint32_t a1[16], a2[16], a3[16], a4[16];  // x1..x4 products of tokens c..c+15
         tmem_ld16(tmem + lane_base + c, a1);
         tmem_ld16(tmem + lane_base + TT + c, a2);
+        tmem_ld16(tmem + lane_base + 2 * TT + c, a3);
+        tmem_ld16(tmem + lane_base + 3 * TT + c, a4);
         tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-          part[(c + t) * C::BM + r] = fmaf(__uint_as_float(a2[t]), 0.0625f, __uint_as_float(a1[t]));
+        for (int t = 0; t < 16; ++t) {
+          const float band_a = fmaf(__uint_as_float(a2[t]), 0.0625f, __uint_as_float(a1[t]));
+          const float band_b = fmaf(__uint_as_float(a4[t]), 0.0625f, __uint_as_float(a3[t]));
+          part[(c + t) * C::BM + r] = fmaf(band_b, 6.103515625e-05f, band_a);  // 2^-14
+        }
       }
     } else {
       ok = false;
@@ -409,8 +440,8 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
 
 }  // namespace
 
-// Token tile.  Up to kW8A16F8MaxM = 32 tokens: beyond that the two E4M3 terms
-// of the tile (2 tt x 128 bytes a k-block) outweigh the weight tile they meet,
+// Token tile.  Up to kW8A16F8MaxM = 32 tokens: beyond that the E4M3 terms of
+// the tile (4 tt x 128 bytes a k-block) outweigh the weight tile they meet,
 // and the BF16 path with converted weights is faster.
 int w8a16_f8_tt(int64_t M) { return M <= 16 ? 16 : 32; }
 
@@ -426,7 +457,7 @@ int w8a16_f8_splits(int units, int kblocks, int sms) {
 
 size_t w8a16_f8_workspace(int64_t M, int64_t K) {
   const int64_t tt = w8a16_f8_tt(M), ttiles = (M + tt - 1) / tt;
-  return (size_t)((ttiles * 2 * tt * K + 255) / 256 * 256) + (size_t)((M * 4 + 255) / 256 * 256);
+  return (size_t)((ttiles * kSplitTerms * tt * K + 255) / 256 * 256) + (size_t)((M * 4 + 255) / 256 * 256);
 }
 
 cudaError_t launch_w8a16_f8(const GemmArgs &g, void *ws, const DeviceInfo &dev, cudaStream_t st) {
@@ -434,7 +465,7 @@ cudaError_t launch_w8a16_f8(const GemmArgs &g, void *ws, const DeviceInfo &dev, 
   if (g.qtype != QLIN_E4M3 || g.M > kW8A16F8MaxM) return cudaErrorInvalidValue;
   const int64_t tt = w8a16_f8_tt(g.M), ttiles = (g.M + tt - 1) / tt;
   uint8_t *xs = (uint8_t *)ws;
-  float *xscale = (float *)((uint8_t *)ws + (ttiles * 2 * tt * g.K + 255) / 256 * 256);
+  float *xscale = (float *)((uint8_t *)ws + (ttiles * kSplitTerms * tt * g.K + 255) / 256 * 256);
   return tt == 16 ? launch_tt<16>(g, xs, xscale, dev, st) : launch_tt<32>(g, xs, xscale, dev, st);
 }
 

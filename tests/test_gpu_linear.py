@@ -112,8 +112,8 @@ def test_w8a16_reads_weights_quantized_just_before(capi, qt, M):
 
 
 def test_w8a16_e4m3_fp8_path_wide_dynamic_range(capi):
-    """Activations spanning 2^16 within a row: the split keeps every element at
-    least 2^-13.8 of the row's maximum exactly, the rest to 2^-14 of the scale."""
+    """Activations spanning 2^16 within a row: the two-band split keeps every
+    element within 2^-28.8 of the row's maximum exactly."""
     M, K, N = 8, 2048, 1024
     rng = synth.rng_for("test-w8a16", 0, "f8-range", "all")
     w = synth.weights(N, K, rng)
@@ -123,6 +123,65 @@ def test_w8a16_e4m3_fp8_path_wide_dynamic_range(capi):
     q, s = oracle.quantize_weight(oracle.E4M3, w)
     y = run_w8a16(capi, "e4m3", x, q, s, None)
     check_tol(y, oracle.w8a16(oracle.E4M3, x, q, s, None), "w8a16 e4m3 wide range")
+
+
+def _massive_case(capi, name, M, magnitude, zero_weights, tag):
+    lin = [l for l in synth.workload(synth.DECODE7B).linears if l.name == name and l.M == 1][0]
+    K, N = lin.K, lin.N
+    rng = synth.rng_for("test-w8a16", 0, f"massive-{name}-{M}-{magnitude}-{zero_weights}-{tag}", "all")
+    w = synth.weights(N, K, rng)
+    xf = synth.bf16_bits_to_f32(synth.activations(M, K, rng, synth.outlier_channels(K, rng)))
+    massive = rng.choice(K, size=4, replace=False)
+    sign = np.where(rng.random((M, 4)) < 0.5, -1.0, 1.0).astype(np.float32)
+    xf[:, massive] = sign * np.float32(magnitude) * (1.0 + rng.random((M, 4))).astype(np.float32)
+    if zero_weights:
+        w[:, massive] = 0.0
+    x = synth.f32_to_bf16_bits(xf)
+    q, s = oracle.quantize_weight(oracle.E4M3, w)
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, "e4m3", M, K, N).startswith("k_w8a16_split+")
+    y = run_w8a16(capi, "e4m3", x, q, s, None)
+    return check_tol(y, oracle.w8a16(oracle.E4M3, x, q, s, None), f"massive {name} M={M} 2^{np.log2(magnitude):.0f}")
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+@pytest.mark.parametrize("name", ["q_proj", "gate_up_proj", "down_proj"])
+def test_w8a16_e4m3_massive_activations_zero_weights(capi, name, M):
+    """Rows with "massive activations": four channels 2^20 above the rest (N(0,1)
+    plus 1 % outlier channels x20) whose weight codes are all zero, so the
+    ordinary elements alone decide y.  The split's band B holds every ordinary
+    element exactly; with band A alone they would keep only about two bits."""
+    _massive_case(capi, name, M, 2.0 ** 20, True, "z20")
+
+
+@pytest.mark.parametrize("M", [1, 32])
+@pytest.mark.parametrize("magnitude", [2.0 ** 10, 2.0 ** 14, 2.0 ** 18])
+def test_w8a16_e4m3_massive_activations_span(capi, M, magnitude):
+    """Massive channels from 2^10 to 2^18 above the rest, zero weights on them."""
+    _massive_case(capi, "q_proj", M, magnitude, True, "span")
+
+
+@pytest.mark.parametrize("M", [1, 32])
+def test_w8a16_e4m3_massive_activations_live_weights(capi, M):
+    """Massive channels 2^18 above the rest with ordinary weights: y is dominated
+    by them and still within tolerance."""
+    _massive_case(capi, "q_proj", M, 2.0 ** 18, False, "live")
+
+
+def test_w8a16_e4m3_split_exact_window(capi):
+    """Ordinary elements spread over 28 binades (N(0,1) times 2^U(-28, 0)), and
+    channel 0 at 448 * 2^-r in row r, so the rows' scales and the place of
+    their elements in the two bands vary row by row; every element within
+    2^-28.8 of its row's maximum is represented exactly."""
+    M, K, N = 24, 2048, 512
+    rng = synth.rng_for("test-w8a16", 0, "f8-window", "all")
+    w = synth.weights(N, K, rng)
+    xf = synth.bf16_bits_to_f32(synth.activations(M, K, rng))
+    xf = xf * np.exp2(rng.uniform(-28.0, 0.0, size=xf.shape)).astype(np.float32)
+    xf[:, 0] = np.float32(448.0) * np.exp2(-np.arange(M, dtype=np.float32))
+    x = synth.f32_to_bf16_bits(xf)
+    q, s = oracle.quantize_weight(oracle.E4M3, w)
+    y = run_w8a16(capi, "e4m3", x, q, s, None)
+    check_tol(y, oracle.w8a16(oracle.E4M3, x, q, s, None), "w8a16 e4m3 exact window")
 
 
 @pytest.mark.parametrize("M", [1, 16])
@@ -220,19 +279,55 @@ def test_w8a8_int8_3b_workload(capi, idx):
     check_tol(y if rows is None else y[rows], ref, f"3b {lin.name} M={lin.M}")
 
 
-@pytest.mark.parametrize("M", [1024, 4096])
+@pytest.mark.parametrize("M", [1024, 4096, 16384, 32640])
 @pytest.mark.parametrize("K,N", [(2048, 11008), (11008, 2048), (2048, 2048)])
 def test_w8a8_e4m3_prefill(capi, M, K, N):
-    """FP8-E4M3 W8A8 static prefill shapes (M up to 4096 here; the largest M are
-    in the slow set), sampled output rows."""
+    """FP8-E4M3 W8A8 static prefill workload, every shape at full size, sampled
+    output rows.  K = 11008 -> 2048 from 16384 tokens on takes the GEMM that
+    quantizes its activations itself; the other shapes quantize in a separate
+    pass."""
     lin = [l for l in synth.workload(synth.PREFILL).linears if l.M == M and l.K == K and l.N == N][0]
+    fused = M >= 16384 and K == 11008
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, "e4m3", M, K, N) == \
+        ("k_fp8_gemm<xq>" if fused else "k_quantize_act+k_fp8_gemm")
     t, q, s = _operands(lin)
     sx = oracle.act_scale(oracle.E4M3, t["cal"])
     y = run_w8a8(capi, "e4m3", t["x"], sx, q, s, None)
-    rows = sample_rows(M, 16)
+    rows = sample_rows(M, 24)
     qx = oracle.quantize_act(oracle.E4M3, t["x"][rows], sx)
     ref = oracle.w8a8(oracle.E4M3, qx, sx, q, s)
     check_tol(y[rows], ref, f"prefill {M}x{K}x{N}")
+
+
+# ------------------------------------------- 36-layer 3B stack, unmerged
+STACK_SHAPES = [("q_proj", 2048, 2048), ("k_proj", 2048, 256), ("gate_up_proj", 2048, 22016),
+                ("down_proj", 11008, 2048)]  # o_proj is q_proj's shape, v_proj k_proj's
+
+
+@pytest.mark.parametrize("name,K,N", STACK_SHAPES)
+def test_stack_decode_int8_w8a16(capi, name, K, N):
+    """The 3B stack's decode linears (INT8 W8A16, 256 tokens), layer 0's
+    tensors, sampled output rows."""
+    lin = [l for l in synth.stack_linears("decode") if l.layer == 0 and l.name == name][0]
+    assert (lin.K, lin.N, lin.M) == (K, N, 256)
+    t, q, s = _operands(lin)
+    y = run_w8a16(capi, "int8", t["x"], q, s, None)
+    rows = sample_rows(lin.M, 32)
+    check_tol(y[rows], oracle.w8a16(oracle.INT8, t["x"], q, s, rows=rows), f"stack decode {name}")
+
+
+@pytest.mark.parametrize("name,K,N", STACK_SHAPES)
+def test_stack_prefill_e4m3_w8a8(capi, name, K, N):
+    """The 3B stack's prefill linears (E4M3 W8A8 static, 8192 tokens), layer
+    0's tensors, sampled output rows."""
+    lin = [l for l in synth.stack_linears("prefill") if l.layer == 0 and l.name == name][0]
+    assert (lin.K, lin.N, lin.M) == (K, N, 8192)
+    t, q, s = _operands(lin)
+    sx = oracle.act_scale(oracle.E4M3, t["cal"])
+    y = run_w8a8(capi, "e4m3", t["x"], sx, q, s, None)
+    rows = sample_rows(lin.M, 24)
+    ref = oracle.w8a8(oracle.E4M3, oracle.quantize_act(oracle.E4M3, t["x"][rows], sx), sx, q, s)
+    check_tol(y[rows], ref, f"stack prefill {name}")
 
 
 @pytest.mark.parametrize("qt", ["int8", "e4m3"])
