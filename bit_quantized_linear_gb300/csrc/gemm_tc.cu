@@ -822,8 +822,14 @@ __global__ void __launch_bounds__(640, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
-  pdl_trigger();
+  // Every role but the weight producer waits for the previous kernel of the
+  // stream here.  Weight codes are never written by a kernel that lets this one
+  // start early (the weight quantizer lets no later kernel start before it
+  // completes), so the weight tiles stream from the start.
+  if (warp != 0) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   if (warp == 0) {  // ------------------------ weight-tile producer
     if (lane == 0) {

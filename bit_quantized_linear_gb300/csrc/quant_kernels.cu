@@ -17,8 +17,10 @@ template <int QT>
 __global__ void __launch_bounds__(256) k_quantize_weight(const float *__restrict__ w,
                                                          uint8_t *__restrict__ q,
                                                          float *__restrict__ s, int64_t K) {
+  // No early start of the next kernel: the linears read their weight codes
+  // before they wait for their predecessor, so the kernel that writes codes
+  // must have completed before any kernel after it begins.
   pdl_wait();
-  pdl_trigger();
   __shared__ float red[8];
   const int64_t n = blockIdx.x;
   const float4 *row = reinterpret_cast<const float4 *>(w + n * K);

@@ -51,12 +51,6 @@ using namespace tc;
 namespace {
 
 // ------------------------------------------------------------ activation split
-// Token row m, chunk c of kSplitChunk elements: one CTA.  Every CTA of a row
-// reads the whole row for its abs-max (the row is small and L2-resident; all of
-// a thread's loads are issued before any is used) and keeps its own chunk in
-// registers, then writes that chunk's four E4M3 terms into the B-operand
-// layout: token tile j (tt tokens) owns rows [4 tt j, 4 tt j + 4 tt) of xs,
-// the x1 rows of its tokens first, then x2, x3 and x4.
 constexpr int kSplitThreads = 256, kSplitChunk = 8 * kSplitThreads, kSplitMaxLoads = 16;
 constexpr int kSplitTerms = 4;  // x1, x2 (band A) and x3, x4 (band B)
 
@@ -80,6 +74,34 @@ __device__ __forceinline__ float absmax8(uint4 v) {
   return a;
 }
 
+// The two-band split of two BF16 values (one 32-bit word) scaled by r = 1/s (a
+// power of two, so x * r is exact): c[q] holds the two codes of term q + 1
+// (element 0 in the low byte).
+__device__ __forceinline__ void split_pair(uint32_t word, float r, uint32_t (&c)[kSplitTerms]) {
+  float v[2] = {bf16_bits_to_f32(word & 0xFFFFu) * r, bf16_bits_to_f32(word >> 16) * r};
+  // band B: the element scaled by 2^14 (exact), split the same way into x3, x4
+  bool lo[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    lo[h] = fabsf(v[h]) < 0.015625f;  // |v| < 2^-6
+    if (lo[h]) v[h] *= 16384.0f;
+  }
+  const __nv_fp8x2_storage_t h1 = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
+  const float2 f1 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h1, __NV_E4M3)));
+  // the remainders are exact in fp32; times 16 they fit E4M3 (see the file's head)
+  const __nv_fp8x2_storage_t h2 =
+      __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v[0] - f1.x), 16.0f * (v[1] - f1.y)), __NV_SATFINITE, __NV_E4M3);
+  // each element's two codes go to its band's pair of terms, zero to the other pair
+  const uint32_t a = (lo[0] ? 0x0000u : 0x00FFu) | (lo[1] ? 0x0000u : 0xFF00u), b = ~a & 0xFFFFu;
+  c[0] = (uint32_t)h1 & a, c[1] = (uint32_t)h2 & a, c[2] = (uint32_t)h1 & b, c[3] = (uint32_t)h2 & b;
+}
+
+// Token row m, chunk c of kSplitChunk elements: one CTA.  Every CTA of a row
+// reads the whole row for its abs-max (the row is small and L2-resident; all of
+// a thread's loads are issued before any is used) and keeps its own chunk in
+// registers, then writes that chunk's four E4M3 terms into the B-operand
+// layout: token tile j (tt tokens) owns rows [4 tt j, 4 tt j + 4 tt) of xs,
+// the x1 rows of its tokens first, then x2, x3 and x4.
 __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *__restrict__ x, int M, int K,
                                                                int tt, uint8_t *__restrict__ xs,
                                                                float *__restrict__ xscale) {
@@ -87,7 +109,7 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
   // The FP8 linear that follows may start at once: before its own wait for this
   // kernel it only arms barriers and loads weight tiles, so its CTAs take the
   // SMs that the previous linear frees during its tail.  Nothing here is
-  // written before the previous kernel has completed.
+  // read or written before the previous kernel has completed.
   pdl_trigger();
   pdl_wait();
   const int m = blockIdx.y, n8 = K / 8;  // K % 16 == 0
@@ -122,32 +144,13 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
   uint8_t *x1 = xs + ((size_t)kSplitTerms * tt * j + t) * K;
   const size_t term = (size_t)tt * K;  // x2, x3, x4 follow, tt rows apart
   const uint32_t w[4] = {own.x, own.y, own.z, own.w};
-  uint32_t c[kSplitTerms][4];  // codes of x1..x4, two per 16 bits
+  uint32_t c[4][kSplitTerms];  // codes of the four words' terms, two per 16 bits
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    float v[2] = {bf16_bits_to_f32(w[e] & 0xFFFFu) * r, bf16_bits_to_f32(w[e] >> 16) * r};  // exact
-    // band B: the element scaled by 2^14 (exact), split the same way into x3, x4
-    bool lo[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      lo[h] = fabsf(v[h]) < 0.015625f;  // |v| < 2^-6
-      if (lo[h]) v[h] *= 16384.0f;
-    }
-    const __nv_fp8x2_storage_t h1 = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
-    const float2 f1 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h1, __NV_E4M3)));
-    // the remainders are exact in fp32; times 16 they fit E4M3 (see the file's head)
-    const __nv_fp8x2_storage_t h2 =
-        __nv_cvt_float2_to_fp8x2(make_float2(16.0f * (v[0] - f1.x), 16.0f * (v[1] - f1.y)), __NV_SATFINITE, __NV_E4M3);
-    // each element's two codes go to its band's pair of terms, zero to the other pair
-    const uint32_t m0 = lo[0] ? 0x0000u : 0x00FFu, m1 = lo[1] ? 0x0000u : 0xFF00u;
-    const uint32_t a1 = (uint32_t)h1 & (m0 | m1), a2 = (uint32_t)h2 & (m0 | m1);
-    const uint32_t b1 = (uint32_t)h1 & (~(m0 | m1) & 0xFFFFu), b2 = (uint32_t)h2 & (~(m0 | m1) & 0xFFFFu);
-    c[0][e] = a1, c[1][e] = a2, c[2][e] = b1, c[3][e] = b2;
-  }
+  for (int e = 0; e < 4; ++e) split_pair(w[e], r, c[e]);
 #pragma unroll
   for (int q = 0; q < kSplitTerms; ++q)
     *reinterpret_cast<uint2 *>(x1 + q * term + 8 * mine) =
-        make_uint2(c[q][0] | (c[q][1] << 16), c[q][2] | (c[q][3] << 16));
+        make_uint2(c[0][q] | (c[1][q] << 16), c[2][q] | (c[3][q] << 16));
 }
 
 // ------------------------------------------------------------ the FP8 linear
@@ -158,12 +161,17 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
 // leaves its fp32 partial tile in shared memory (the drained ring) and the
 // cluster sums them in rank order through distributed shared memory, each CTA
 // finishing a slice of the outputs.
-template <int TT>  // token tile; the MMA's N is 4 TT (the four terms of each token)
+// The B operand (the four E4M3 terms of every token of the tile) comes from
+// k_w8a16_split through the workspace, with one power-of-two scale per token
+// row; the epilogue folds that scale into the partial tile, so the cluster's
+// sum of the partials needs no per-token factor.
+template <int TT>
 struct W8F8Cfg {
   static constexpr int BM = 128, BK = 128, NB = kSplitTerms * TT;
-  static constexpr int A_BYTES = BM * BK, B_BYTES = NB * BK, STAGE = A_BYTES + B_BYTES;
-  // The ring depth is a launch parameter (stages of STAGE bytes; the barriers
-  // follow the ring).
+  static constexpr int A_BYTES = BM * BK, B_BYTES = NB * BK;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  // The ring depth is a launch parameter (stages of STAGE bytes); the barriers
+  // follow the ring.
   static constexpr int MAX_STAGES = 14, BAR_BYTES = 256;
   static constexpr int PART_BYTES = TT * BM * 4;  // [TT tokens][BM rows] fp32, in the drained ring
   static constexpr int THREADS = 192;
@@ -188,11 +196,6 @@ struct W8F8Params {
 
 __device__ __forceinline__ uint8_t *align1k(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 template <int TT>
@@ -249,34 +252,30 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
       auto load_x = [&](int i) {
         tma_load_2d(&tm_x, &full[i % NS], smem + (i % NS) * C::STAGE + C::A_BYTES, (kb0 + i) * C::BK, tj * C::NB);
       };
-      // Before the wait for the split (and, through it, for every earlier kernel
-      // of the stream) only L2 prefetches of the first weight tiles are issued.
-      // An earlier kernel may still be writing these weights, and a prefetch into
-      // the coherent L2 cannot hand a stale byte to the MMAs.  Every load into
-      // shared memory follows the wait.
+      // The weight tiles of the first stages are loaded before the wait for the
+      // previous kernel: weight codes are never written by a kernel that lets
+      // this one start early (the weight quantizer lets no later kernel start
+      // before it completes).  The activation terms follow the wait.
       const int pre = nkb < NS ? nkb : NS;
       for (int i = 0; i < pre; ++i) {
-        const int k = (kb0 + i) * C::BK;
-        if (p.glu) {
-          tma_prefetch_l2_2d(&tm_w, k, tile * 64);
-          tma_prefetch_l2_2d(&tm_w, k, p.N + tile * 64);
-        } else {
-          tma_prefetch_l2_2d(&tm_w, k, tile * C::BM);
-        }
+        mbar_arrive_expect_tx(&full[i], C::STAGE);
+        load_w(i);
       }
       pdl_wait();
       int i = 0;
       for (; i < nkb; ++i) {
         const int s = i % NS;
-        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
-          *abort_flag = 1;
-          break;
+        if (i >= NS) {
+          if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          load_w(i);
         }
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        load_w(i);
         load_x(i);
       }
-      if (*abort_flag) drain_ring(full, NS, i, NS);  // armed stages land before the CTA leaves
+      if (*abort_flag) drain_ring(full, NS, i > pre ? i : pre, NS);  // armed stages land before the CTA leaves
     }
   } else if (warp == 1) {  // ------------------------ MMA issuer
     if (lane == 0) {
@@ -304,7 +303,10 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   } else {  // ------------------------------------- epilogue: accumulators -> partial tile
     const int q4 = warp & 3, r = q4 * 32 + lane;  // TMEM lane = weight row of the tile
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    bool ok = mbar_wait(acc_full, 0, abort_flag);
+    bool ok = true;
+    pdl_wait();  // the split's scales are complete from here on
+    const int m0 = tj * TT;
+    ok = ok && mbar_wait(acc_full, 0, abort_flag);
     tc_fence_after();
     if (__all_sync(0xffffffffu, ok && !*abort_flag)) {  // tcgen05.ld is warp-collective
       float *part = reinterpret_cast<float *>(smem);   // the ring is drained: every MMA has read it
@@ -318,9 +320,11 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
+          const int m = m0 + c + t;
+          const float sx = m < p.M ? __ldg(p.x_scale + m) : 0.0f;  // the token row's scale
           const float band_a = fmaf(__uint_as_float(a2[t]), 0.0625f, __uint_as_float(a1[t]));
           const float band_b = fmaf(__uint_as_float(a4[t]), 0.0625f, __uint_as_float(a3[t]));
-          part[(c + t) * C::BM + r] = fmaf(band_b, 6.103515625e-05f, band_a);  // 2^-14
+          part[(c + t) * C::BM + r] = sx * fmaf(band_b, 6.103515625e-05f, band_a);  // 2^-14
         }
       }
     } else {
@@ -333,36 +337,58 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   if (S > 1) cluster_sync();  // every partial tile of the cluster is written
 
   // ------------------------------------------- sum over the splits, finish the outputs
-  // this CTA finishes elements [e0, e1) of the tile; consecutive threads take
-  // consecutive rows (channels) of one token, so the stores are coalesced
-  pdl_wait();  // x_scale and y belong to the previous kernels from here on
+  // this CTA finishes items [e0, e1) of the tile: an item is 4 consecutive rows
+  // (channels) of one token, read as one 16-byte piece from each CTA of the
+  // cluster in rank order (deterministic); consecutive threads take consecutive
+  // items of one token, so the stores are coalesced
+  pdl_wait();  // y belongs to the previous kernels from here on
   {
-    const int rows = p.glu ? 64 : C::BM, E = TT * rows;
+    const int rows = p.glu ? 64 : C::BM, R4 = rows / 4, E = TT * R4;
     const int e0 = split * E / S, e1 = (split + 1) * E / S;
     const uint32_t pbase = smem_u32(smem);
+    auto sum4 = [&](int t, int row) {
+      const uint32_t a = pbase + 4u * (uint32_t)(t * C::BM + row);
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (S == 1) return *reinterpret_cast<const float4 *>(smem + 4 * (t * C::BM + row));
+      for (int q = 0; q < S; ++q) {  // fixed order
+        const uint4 u = ld_dsmem_v4(map_peer_smem(a, (uint32_t)q));
+        v.x += __uint_as_float(u.x), v.y += __uint_as_float(u.y), v.z += __uint_as_float(u.z),
+            v.w += __uint_as_float(u.w);
+      }
+      return v;
+    };
     for (int e = e0 + (int)threadIdx.x; e < e1; e += C::THREADS) {
-      const int t = e / rows, rr = e % rows, m = tj * TT + t;
+      const int t = e / R4, rr = (e - t * R4) * 4, m = tj * TT + t;
       if (m >= p.M) continue;
-      auto sum_at = [&](int row) {
-        const uint32_t a = pbase + 4u * (uint32_t)(t * C::BM + row);
-        if (S == 1) return *reinterpret_cast<const float *>(smem + 4 * (t * C::BM + row));
-        float v = 0.0f;
-        for (int q = 0; q < S; ++q) v += ld_dsmem_f32(map_peer_smem(a, (uint32_t)q));  // fixed order
-        return v;
-      };
-      const float sx = __ldg(p.x_scale + m);
       if (p.glu) {
         const int n = tile * 64 + rr;
-        const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
-        const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + n)) : 0.0f;
-        const float g = fmaf(sum_at(rr), sx * __ldg(p.w_scale + n), bg);
-        const float u = fmaf(sum_at(64 + rr), sx * __ldg(p.w_scale + p.N + n), bu);
-        p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(silu_f(g) * u);
+        const float4 g4 = sum4(t, rr), u4 = sum4(t, 64 + rr);
+        const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, us[4] = {u4.x, u4.y, u4.z, u4.w};
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n + i)) : 0.0f;
+          const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + n + i)) : 0.0f;
+          const float g = fmaf(gs[i], __ldg(p.w_scale + n + i), bg);
+          const float u = fmaf(us[i], __ldg(p.w_scale + p.N + n + i), bu);
+          o[i] = silu_f(g) * u;
+        }
+        *reinterpret_cast<uint2 *>(p.y + (size_t)m * p.N + n) =
+            make_uint2(f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
+                       f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
       } else {
         const int n = tile * C::BM + rr;
-        if (n >= p.N) continue;
-        const float b = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n)) : 0.0f;
-        p.y[(size_t)m * p.N + n] = f32_to_bf16_bits(fmaf(sum_at(rr), sx * __ldg(p.w_scale + n), b));
+        if (n >= p.N) continue;  // N % 16 == 0: the four channels are all in or all out
+        const float4 v4 = sum4(t, rr);
+        const float vs[4] = {v4.x, v4.y, v4.z, v4.w};
+        const float4 ws = __ldg(reinterpret_cast<const float4 *>(p.w_scale + n));
+        const float sw[4] = {ws.x, ws.y, ws.z, ws.w};
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = fmaf(vs[i], sw[i], p.bias ? bf16_bits_to_f32(__ldg(p.bias + n + i)) : 0.0f);
+        *reinterpret_cast<uint2 *>(p.y + (size_t)m * p.N + n) =
+            make_uint2(f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
+                       f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
       }
     }
   }
@@ -401,6 +427,9 @@ bool map_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, uint3
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Shared memory of one CTA when two share an SM (228 KB, 1 KB of it reserved per CTA).
+constexpr int kCtaSmem = 113 * 1024;
+
 template <int TT>
 cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const DeviceInfo &dev, cudaStream_t st) {
   using C = W8F8Cfg<TT>;
@@ -421,18 +450,19 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
   p.ntiles = g.glu ? (int)(g.N / 64) : (int)((g.N + C::BM - 1) / C::BM);
   const int units = p.ntiles * ttiles, KB = (int)((g.K + C::BK - 1) / C::BK);
   p.splits = w8a16_f8_splits(units, KB, dev.sms);
-  // two CTAs to an SM, each with about 108 KB of ring
-  constexpr int kShared = 108 * 1024;
-  constexpr int max_stages = kShared / C::STAGE < C::MAX_STAGES ? kShared / C::STAGE : C::MAX_STAGES;
+  // two CTAs to an SM: as many stages as fit beside the barriers
+  constexpr int fit = (kCtaSmem - C::smem_bytes(0)) / C::STAGE;
+  constexpr int max_stages = fit < C::MAX_STAGES ? fit : C::MAX_STAGES;
+  static_assert(max_stages >= 3, "ring depth");
   p.stages = max_stages;
   p.w_scale = g.w_scale;
   p.x_scale = xscale;
   p.bias = g.bias;
   p.y = (uint16_t *)g.y;
   p.status = dev.status;
-  static_assert(C::smem_bytes(max_stages) <= 227 * 1024, "shared memory");
-  static const cudaError_t attr = cudaFuncSetAttribute(k_w8a16_f8<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       C::smem_bytes(max_stages));
+  static_assert(C::smem_bytes(max_stages) <= kCtaSmem, "shared memory");
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_w8a16_f8<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes(max_stages));
   if (attr != cudaSuccess) return attr;
   return launch_kernel(k_w8a16_f8<TT>, dim3((unsigned)units, 1, (unsigned)p.splits), dim3(C::THREADS),
                        C::smem_bytes(p.stages), st, (unsigned)p.splits, tw, tx, p);

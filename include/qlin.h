@@ -31,9 +31,13 @@
  *   - Calls on one stream are ordered like any work on it.  A call sees
  *     everything earlier work on the stream wrote, weights included, and
  *     later work sees its outputs.  Consecutive kernels of the library start
- *     early (programmatic dependent launch).  Before a kernel's wait for its
- *     predecessor it only prefetches weights into the coherent L2, so an
- *     overlapping predecessor can never make it read stale data.
+ *     early (programmatic dependent launch): a kernel's CTAs take SMs while its
+ *     predecessor finishes, and wait for it before they read its outputs.  The
+ *     one input read before that wait is a linear's weight codes (`qw`).  So a
+ *     buffer of weight codes must not be the output of the library call right
+ *     before the linear on its stream, other than qlin_quantize_weight (which
+ *     lets no later kernel start before it completes).  Codes written by any
+ *     other kernel or copy, or by any earlier call, are read as written.
  *   - Argument errors are detected on the host before anything is launched and
  *     returned as a status: NULL required pointer, negative sizes, K or N not a
  *     multiple of 16, pointers not 16-byte aligned, unknown qtype, workspace
