@@ -113,14 +113,19 @@ constexpr int kXqPrefetch = 0;  // chunks brought into L2 ahead of the staging r
 // there, 48 KB, would buy the quantizer three more chunks of staging).
 constexpr int kFp8XqStages = 4;
 
-template <int XQ>
+// PAIR = 1: the two CTAs of a 2-CTA cluster compute a 256 x 256 tile with
+// pair MMAs (cta_group::2): each CTA stages its own 128 tokens of A and 128 of
+// the 256 channels of B, so a stage is 32 KB instead of 48 KB, and the MMA
+// reads each CTA's B half once for both CTAs' rows.
+template <int XQ, int PAIR = 0>
 struct Fp8CfgT {
-  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages : 4;
-  static constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
-  // epilogue: one 32 x 32 BF16 block per epilogue warp, staged for a TMA store
-  // (XQ: stored directly by rows, the shared memory holds the activation ring)
+  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages + PAIR : PAIR ? 6 : 4;
+  static constexpr int A_BYTES = BM * BK, B_BYTES = (PAIR ? BN / 2 : BN) * BK, STAGE_BYTES = A_BYTES + B_BYTES;
+  // epilogue: two 32 x 32 BF16 blocks per epilogue warp, staged for TMA stores
+  // (one fills while the other's store reads it; XQ: stored directly by rows,
+  // the shared memory holds the activation ring)
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES, EPI_WARP_BYTES = 32 * 32 * 2;
-  static constexpr int EPI_BYTES = XQ ? 0 : 8 * EPI_WARP_BYTES;
+  static constexpr int EPI_BYTES = XQ ? 0 : 8 * 2 * EPI_WARP_BYTES;
   // XQ: a ring of chunks (XQ_ROWS rows of a task's 128 x 128 BF16 activation
   // tile), TMA-staged, as many as the rest of the shared memory holds
   static constexpr int XQ_ROWS = 64, XQ_CPT = BM / XQ_ROWS, XQ_CHUNK = XQ_ROWS * BK * 2;
@@ -129,7 +134,7 @@ struct Fp8CfgT {
   static constexpr int BAR_OFF = XQ_OFF + XQ_NBUF * XQ_CHUNK;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr int THREADS = XQ ? 512 : 384;
-  static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, BN);
+  static constexpr uint32_t IDESC = umma_idesc(0, 0, PAIR ? 2 * BM : BM, BN);
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(XQ == 0 || (XQ_NBUF >= 2 && XQ_NBUF <= 6), "chunk ring (barriers and counters at BAR_OFF + 128)");
 };
@@ -148,11 +153,18 @@ using Fp8Cfg = Fp8CfgT<0>;
 // async proxy after either acquire.  The quantization streams from HBM while
 // the GEMM is bound by the tensor cores and L2, so it overlaps.  The launch is
 // cooperative: every CTA is resident, and every wait is bounded besides.
-template <int XQ>
-__global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
+//
+// PAIR = 1 (2-CTA clusters): work items are pair tiles, 256 tokens (m-tiles 2q
+// and 2q + 1, one per CTA) by 256 channels (128 per CTA).  Only the even CTA
+// issues MMAs.  Both CTAs' TMA loads count their bytes on the even CTA's full
+// barrier; the MMA commits arrive on the empty and accumulator barriers of both
+// CTAs; both CTAs' epilogue warps release an accumulator on the even CTA's
+// barrier.  Each CTA's tensor memory holds its own 128 tokens of the tile.
+template <int XQ, int PAIR>
+__global__ void __launch_bounds__(Fp8CfgT<XQ, PAIR>::THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, Fp8Params p) {
-  using C = Fp8CfgT<XQ>;
+  using C = Fp8CfgT<XQ, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint64_t *full = (uint64_t *)(smem + C::BAR_OFF);
@@ -162,11 +174,26 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (p.K + C::BK - 1) / C::BK;
-  // output tiles t = blockIdx.x + j * gridDim.x, m-tile major
-  const int items = p.mtiles * p.ntiles, G = gridDim.x, cid = blockIdx.x;
+  if constexpr (PAIR) {
+    // Launched without its 2-CTA cluster shape, the pair MMAs, loads and barrier
+    // arrivals would address a CTA that does not exist: report and leave before
+    // any barrier, tensor memory or peer is touched.
+    if (cluster_nctarank() != 2) {
+      if (threadIdx.x == 0) set_status(p.status, QLIN_ERR_UNSUPPORTED);
+      return;
+    }
+  }
+  const int rank = PAIR ? (int)(cluster_ctarank() & 1u) : 0;
+  // work items t = cid + j * G, m-group major: output tiles, or pair tiles
+  // (m-tiles 2q, 2q + 1 of one n-tile)
+  const int mgroups = PAIR ? (p.mtiles + 1) / 2 : p.mtiles;
+  const int items = mgroups * p.ntiles, G = gridDim.x / (PAIR + 1), cid = blockIdx.x / (PAIR + 1);
   const int my_tiles = (cid < items) ? (items - cid + G - 1) / G : 0;
-  auto tile_m0 = [&](int t) { return (t / p.ntiles) * C::BM; };
+  auto tile_m0 = [&](int t) { return ((t / p.ntiles) * (PAIR + 1) + rank) * C::BM; };
   auto tile_n0 = [&](int t) { return (t % p.ntiles) * C::BN; };
+  // the even CTA's barrier at the same offset as `bar` (shared::cluster address)
+  auto leader = [&](uint64_t *bar) { return PAIR ? map_peer_smem(smem_u32(bar), 0) : smem_u32(bar); };
+  auto peer = [&](uint64_t *bar) { return map_peer_smem(smem_u32(bar), 1); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -175,7 +202,7 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);  // the eight epilogue warps
+      mbar_init(&acc_empty[b], PAIR ? 16 : 8);  // the epilogue warps (of both CTAs of a pair)
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -193,15 +220,27 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
       tma_prefetch_desc(&tm_x);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(tmem_slot, 512);
+    else tmem_alloc(tmem_slot, 512);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  bool pair_ok = true;
+  if constexpr (PAIR) {
+    cluster_sync();  // both CTAs' barriers exist before a load, commit or arrival reaches them
+    // both CTAs must hold the same tensor-memory address; otherwise neither does any work
+    pair_ok = ld_dsmem_u32(map_peer_smem(smem_u32(tmem_slot), (uint32_t)(rank ^ 1))) == tmem;
+    if (!pair_ok && threadIdx.x == 0) set_status(p.status, QLIN_ERR_UNSUPPORTED);
+  }
   pdl_wait();  // inputs of the previous kernel in the stream are complete from here on
   pdl_trigger();
 
-  if (warp == 0) {  // ------------------------------- TMA producer
+  if (!pair_ok) {
+    // a pair whose tensor memory does not match does nothing but leave together
+  } else if (warp == 0) {  // ------------------------------- TMA producer
     if (lane == 0) {
       int i = 0;
       // XQ: the tiles of bands 0..ready_band (seen complete, fenced once) load
@@ -261,16 +300,29 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
             break;
           }
           uint8_t *st = smem + s * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          tma_load_2d(&tm_a, &full[s], st, kb * C::BK, m0);
           // B: two boxes of 128 rows; glu: the gate rows n0/2.. and the matching up rows N + n0/2..
           const int b0 = p.glu ? n0 / 2 : n0, b1 = p.glu ? p.N + n0 / 2 : n0 + C::BN / 2;
-          tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, b0);
-          tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, b1);
+          if constexpr (PAIR) {  // this CTA's A tile and its B box; both CTAs' bytes count on the even CTA
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+            const uint32_t fb = leader(&full[s]);
+            tma_load_2d_pair(&tm_a, fb, st, kb * C::BK, m0);
+            tma_load_2d_pair(&tm_b, fb, st + C::A_BYTES, kb * C::BK, rank ? b1 : b0);
+          } else {
+            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+            tma_load_2d(&tm_a, &full[s], st, kb * C::BK, m0);
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES, kb * C::BK, b0);
+            tma_load_2d(&tm_b, &full[s], st + C::A_BYTES + C::B_BYTES / 2, kb * C::BK, b1);
+          }
         }
       }
-      // abort: the stages this CTA armed land before it leaves
-      if (*abort_flag) drain_ring(full, C::STAGES, i, C::STAGES);
+      if constexpr (PAIR) {
+        // the last stages this CTA loaded have been read by the pair's MMAs (the
+        // empty barriers the MMA commits arrive on) before it leaves
+        for (int k = i > C::STAGES ? i - C::STAGES : 0; k < i; ++k)
+          mbar_wait_drain(&empty[k % C::STAGES], (uint32_t)(k / C::STAGES) & 1);
+      } else if (*abort_flag) {
+        drain_ring(full, C::STAGES, i, C::STAGES);  // abort: the stages this CTA armed land before it leaves
+      }
     }
   } else if (XQ == 1 && (warp == 2 || warp == 3 || warp >= 12)) {  // ----- activation quantizer
     uint64_t *xq_full = (uint64_t *)(smem + C::BAR_OFF + 128), *xq_empty = xq_full + C::XQ_NBUF;
@@ -397,8 +449,8 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {  // ------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1) {  // ------------------------ MMA issuer (the even CTA of a pair)
+    if (lane == 0 && rank == 0) {
       bool ok = true;
       int i = 0;
       for (int j = 0; j < my_tiles && ok; ++j) {
@@ -418,14 +470,28 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
           tc_fence_after();
           const uint32_t a = smem_u32(smem + s * C::STAGE_BYTES);
           const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(a + C::A_BYTES);
-          mma_fp8(dt, ad, bd, C::IDESC, kb > 0 ? 1u : 0u);  // K = 32 per instruction (32 bytes)
-          mma_fp8(dt, ad + 2, bd + 2, C::IDESC, 1u);
-          mma_fp8(dt, ad + 4, bd + 4, C::IDESC, 1u);
-          mma_fp8(dt, ad + 6, bd + 6, C::IDESC, 1u);
-          mma_commit(&empty[s]);
+          if constexpr (PAIR) {
+            mma_fp8_pair(dt, ad, bd, C::IDESC, kb > 0 ? 1u : 0u);  // K = 32 per instruction (32 bytes)
+            mma_fp8_pair(dt, ad + 2, bd + 2, C::IDESC, 1u);
+            mma_fp8_pair(dt, ad + 4, bd + 4, C::IDESC, 1u);
+            mma_fp8_pair(dt, ad + 6, bd + 6, C::IDESC, 1u);
+            mma_commit_pair(smem_u32(&empty[s]));
+            mma_commit_pair(peer(&empty[s]));
+          } else {
+            mma_fp8(dt, ad, bd, C::IDESC, kb > 0 ? 1u : 0u);  // K = 32 per instruction (32 bytes)
+            mma_fp8(dt, ad + 2, bd + 2, C::IDESC, 1u);
+            mma_fp8(dt, ad + 4, bd + 4, C::IDESC, 1u);
+            mma_fp8(dt, ad + 6, bd + 6, C::IDESC, 1u);
+            mma_commit(&empty[s]);
+          }
         }
         if (!ok) break;
-        mma_commit(&acc_full[b]);
+        if constexpr (PAIR) {
+          mma_commit_pair(smem_u32(&acc_full[b]));
+          mma_commit_pair(peer(&acc_full[b]));
+        } else {
+          mma_commit(&acc_full[b]);
+        }
       }
       // Drain: no commit arrival may still be in flight towards this CTA's shared
       // memory when it exits (a successor CTA on this SM may already own it); the
@@ -438,13 +504,14 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const float sx = p.xs_per_token ? 1.0f : __ldg(p.x_scale);
     // Output path: each 32 x 32 block of BF16 results (row = lane) is written into
-    // this warp's staging block with the 64-byte swizzle (16-byte chunk q of row r
-    // at chunk q ^ ((r >> 1) & 3): the lanes' row writes hit distinct banks), then
-    // stored by TMA, which writes whole row segments and clips rows and columns
-    // outside y.
-    uint8_t *stage = smem + C::EPI_OFF + (warp - 4) * C::EPI_WARP_BYTES;
-    const uint32_t st_row = smem_u32(stage) + 64u * lane, sw = (lane >> 1) & 3;
-    bool pending = false;  // lane 0 has a store in flight that reads the staging block
+    // one of this warp's two staging blocks with the 64-byte swizzle (16-byte chunk
+    // q of row r at chunk q ^ ((r >> 1) & 3): the lanes' row writes hit distinct
+    // banks), then stored by TMA, which writes whole row segments and clips rows
+    // and columns outside y.  The blocks alternate, so a block is rewritten only
+    // once the store issued two blocks earlier has read it.
+    uint8_t *stage = smem + C::EPI_OFF + (warp - 4) * 2 * C::EPI_WARP_BYTES;
+    const uint32_t sw = (lane >> 1) & 3;
+    int emitted = 0;  // stores lane 0 has issued
     auto emit = [&](const uint32_t (&o)[16], int x, int y) {
       if constexpr (XQ == 1) {  // row stores: lane = row y + lane, columns x..x+31 (64 bytes)
         const int m = y + lane;
@@ -456,20 +523,22 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         }
         return;
       }
-      if (pending) {
-        if (lane == 0) bulk_wait_read_all();
+      uint8_t *blk = stage + (emitted & 1) * C::EPI_WARP_BYTES;
+      if (emitted >= 2) {
+        if (lane == 0) bulk_wait_read_1();  // the store from two blocks ago has read this block
         __syncwarp();
       }
+      const uint32_t st_row = smem_u32(blk) + 64u * lane;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         sts128(st_row + (((uint32_t)q ^ sw) << 4), make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
       fence_proxy_async_smem();  // the TMA store reads the block through the async proxy
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(&tm_y, stage, x, y);
+        tma_store_2d(&tm_y, blk, x, y);
         bulk_commit();
       }
-      pending = true;
+      ++emitted;
     };
     // Column factors of 8 channels from n (the same for every lane: broadcast
     // loads): scale s_x * s_w[n + i] and bias; zero from channel `end` on (n is a
@@ -507,6 +576,16 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
         break;
       }
       const int m = m0 + q4 * 32 + lane, yrow0 = m0 + q4 * 32;
+      // the second m-tile of a pair past M has no rows to write (its loads read zeros)
+      if (m0 >= p.M) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR && rank) mbar_arrive_cluster(leader(&acc_empty[b]));
+          else mbar_arrive(&acc_empty[b]);
+        }
+        continue;
+      }
       // per-token activation scale multiplies the row (lane = token)
       const float sxm = p.xs_per_token ? (m < p.M ? __ldg(p.x_scale + m) : 0.0f) : 1.0f;
       if (p.glu) {
@@ -569,10 +648,13 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      if (lane == 0) {
+        if (PAIR && rank) mbar_arrive_cluster(leader(&acc_empty[b]));
+        else mbar_arrive(&acc_empty[b]);
+      }
     }
     // every store has written y (and read its staging block) before the CTA leaves
-    if (lane == 0 && pending) bulk_wait_all();
+    if (lane == 0 && emitted > 0) bulk_wait_all();
     __syncwarp();
     if (!ok) *abort_flag = 1;
   }
@@ -580,7 +662,19 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if constexpr (PAIR) {
+    // neither CTA frees the pair's tensor memory or leaves while the other may
+    // still send it loads, commits or arrivals (every wait above is bounded, so
+    // both get here); on the abort path what was sent is given time to land
+    cluster_sync();
+    if (*abort_flag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+    }
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+  } else {
+    if (warp == 1) tmem_dealloc(tmem, 512);
+  }
 }
 
 // ========================================== swap-AB GEMM with A in tensor memory
@@ -1306,20 +1400,31 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
     const size_t fb = fp8_xq_flag_bytes(g.M, g.K);
     cudaError_t e = cudaMemsetAsync(g.xq_flags, 0, fb, st);
     if (e != cudaSuccess) return e;
-    using CX = Fp8CfgT<1>;
-    static cudaError_t a1 = set_smem(k_fp8_gemm<1>, CX::SMEM);
+    // CTA pairs (256 x 256 tiles with pair MMAs); cooperative launch of 2-CTA clusters
+    using CX = Fp8CfgT<1, 1>;
+    static cudaError_t a1 = set_smem(k_fp8_gemm<1, 1>, CX::SMEM);
     if (a1 != cudaSuccess) return a1;
-    const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-    // band of quantization tasks: the m-tiles one wave of `grid` tiles spans
-    const int b = (grid + ntiles - 1) / ntiles;
+    const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
+    const int grid = 2 * (items < pairs ? items : pairs);
+    // band of quantization tasks: the m-tiles one wave of grid / 2 pair tiles spans
+    const int b = 2 * ((grid / 2 + ntiles - 1) / ntiles);
     p.xq_band = b < mtiles ? b : mtiles;
-    return launch_kernel_coop(k_fp8_gemm<1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 1, ta, tb, tx,
+    return launch_kernel_coop(k_fp8_gemm<1, 1>, dim3((unsigned)grid), dim3(CX::THREADS), CX::SMEM, st, 2, ta, tb, tx,
                               ty, p);
   }
-  static cudaError_t attr = set_smem(k_fp8_gemm<0>, C::SMEM);
+  if (mtiles >= 2) {  // CTA pairs: 256 x 256 tiles with pair MMAs
+    using CP = Fp8CfgT<0, 1>;
+    static cudaError_t attr2 = set_smem(k_fp8_gemm<0, 1>, CP::SMEM);
+    if (attr2 != cudaSuccess) return attr2;
+    const int items = ((mtiles + 1) / 2) * ntiles, pairs = dev.sms / 2;
+    const int grid = 2 * (items < pairs ? items : pairs);
+    return launch_kernel_x(k_fp8_gemm<0, 1>, dim3((unsigned)grid), dim3(CP::THREADS), CP::SMEM, st, 2, ta, tb, tb, ty,
+                           p);
+  }
+  static cudaError_t attr = set_smem(k_fp8_gemm<0, 0>, C::SMEM);
   if (attr != cudaSuccess) return attr;
   const int tiles = mtiles * ntiles, grid = tiles < dev.sms ? tiles : dev.sms;
-  return launch_kernel(k_fp8_gemm<0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, ty, p);
+  return launch_kernel(k_fp8_gemm<0, 0>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, st, 1, ta, tb, tb, ty, p);
 }
 
 // Token tile (MMA N) of the W8A16 swap-AB kernel.  Up to 128 tokens the tile
@@ -1343,7 +1448,7 @@ size_t fp8_xq_flag_bytes(int64_t M, int64_t K) {
 // tile's main loop is long and the quantization a large share of the work:
 // K >= 4096, at most 4096 GEMM columns, and 64 m-tiles or more (8192 tokens);
 // at K = 2048 the separate pass with the TMA-store epilogue is 20-28% faster.
-// Its quantizers are the GEMM's CTAs, so the output tiles must fill every SM.
+// Its quantizers are the GEMM's CTAs, so the pair tiles must fill every SM.
 // N counts GEMM columns (2I for the merged gate_up).
 // QLIN_FP8_FUSED_QUANT=0 in the environment (read once) keeps the separate
 // quantization pass everywhere, so the two forms can be compared on one shape.
@@ -1354,7 +1459,7 @@ bool fp8_xq_used(int64_t M, int64_t K, int64_t N, int sms) {
   }();
   if (!enabled) return false;
   const int64_t mtiles = (M + Fp8Cfg::BM - 1) / Fp8Cfg::BM, ntiles = (N + Fp8Cfg::BN - 1) / Fp8Cfg::BN;
-  return mtiles >= 64 && K >= 4096 && N <= 4096 && mtiles * ntiles >= sms;
+  return mtiles >= 64 && K >= 4096 && N <= 4096 && ((mtiles + 1) / 2) * ntiles >= sms / 2;
 }
 
 int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms) {
