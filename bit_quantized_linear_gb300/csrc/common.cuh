@@ -25,6 +25,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // BF16 bit pattern -> fp32 (exact).
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
+// Two integer-valued floats of magnitude below 2^8 (8-bit codes) as BF16,
+// packed (lo in the low half).  The binary32 pattern of such a value has zeros
+// in its 16 low bits, so its upper half is the exact BF16 value: one byte
+// permute instead of two conversions.
+__device__ __forceinline__ uint32_t pack_code_bf16x2(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
+
 // fp32 -> BF16 bit pattern, round to nearest even.
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));

@@ -109,8 +109,8 @@ struct Fp8Params {
 constexpr int kXqConverters = 4;
 constexpr int kXqPrefetch = 0;  // chunks brought into L2 ahead of the staging ring
 
-// GEMM pipeline depth of the fused-quantization variant (a stage given up
-// there, 48 KB, would buy the quantizer three more chunks of staging).
+// GEMM pipeline depth of the fused-quantization variant (CTA pairs, 32 KB
+// stages): 4 stages, the output staging and 3 chunks of activation staging.
 constexpr int kFp8XqStages = 4;
 
 // PAIR = 1: the two CTAs of a 2-CTA cluster compute a 256 x 256 tile with
@@ -119,18 +119,18 @@ constexpr int kFp8XqStages = 4;
 // reads each CTA's B half once for both CTAs' rows.
 template <int XQ, int PAIR = 0>
 struct Fp8CfgT {
-  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages + PAIR : PAIR ? 6 : 4;
+  static constexpr int BM = 128, BN = 256, BK = 128, STAGES = XQ ? kFp8XqStages : PAIR ? 6 : 4;
   static constexpr int A_BYTES = BM * BK, B_BYTES = (PAIR ? BN / 2 : BN) * BK, STAGE_BYTES = A_BYTES + B_BYTES;
   // epilogue: two 32 x 32 BF16 blocks per epilogue warp, staged for TMA stores
-  // (one fills while the other's store reads it; XQ: stored directly by rows,
-  // the shared memory holds the activation ring)
+  // (one fills while the other's store reads it)
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES, EPI_WARP_BYTES = 32 * 32 * 2;
-  static constexpr int EPI_BYTES = XQ ? 0 : 8 * 2 * EPI_WARP_BYTES;
+  static constexpr int EPI_BYTES = 8 * 2 * EPI_WARP_BYTES;
   // XQ: a ring of chunks (XQ_ROWS rows of a task's 128 x 128 BF16 activation
   // tile), TMA-staged, as many as the rest of the shared memory holds
   static constexpr int XQ_ROWS = 64, XQ_CPT = BM / XQ_ROWS, XQ_CHUNK = XQ_ROWS * BK * 2;
   static constexpr int XQ_OFF = EPI_OFF + EPI_BYTES;
   static constexpr int XQ_NBUF = XQ ? (227 * 1024 - XQ_OFF - 256 - 1024) / XQ_CHUNK : 0;
+  static_assert(XQ == 0 || PAIR == 1, "the fused-quantization variant runs CTA pairs (32 KB stages)");
   static constexpr int BAR_OFF = XQ_OFF + XQ_NBUF * XQ_CHUNK;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr int THREADS = XQ ? 512 : 384;
@@ -513,16 +513,6 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ, PAIR>::THREADS, 1)
     const uint32_t sw = (lane >> 1) & 3;
     int emitted = 0;  // stores lane 0 has issued
     auto emit = [&](const uint32_t (&o)[16], int x, int y) {
-      if constexpr (XQ == 1) {  // row stores: lane = row y + lane, columns x..x+31 (64 bytes)
-        const int m = y + lane;
-        if (m < p.M) {
-          uint4 *dst = reinterpret_cast<uint4 *>(p.y + (size_t)m * p.N + x);
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            if (x + 8 * g < p.N) dst[g] = make_uint4(o[4 * g], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
-        }
-        return;
-      }
       uint8_t *blk = stage + (emitted & 1) * C::EPI_WARP_BYTES;
       if (emitted >= 2) {
         if (lane == 0) bulk_wait_read_1();  // the store from two blocks ago has read this block
@@ -774,8 +764,8 @@ __device__ __forceinline__ void convert16(uint4 raw, uint32_t *o) {
       const float f1 = __uint_as_float(__byte_perm(u, 0x4Bu, 0x4551)) - 8388736.0f;
       const float f2 = __uint_as_float(__byte_perm(u, 0x4Bu, 0x4552)) - 8388736.0f;
       const float f3 = __uint_as_float(__byte_perm(u, 0x4Bu, 0x4553)) - 8388736.0f;
-      o[2 * i] = pack_bf16x2(f0, f1);
-      o[2 * i + 1] = pack_bf16x2(f2, f3);
+      o[2 * i] = pack_code_bf16x2(f0, f1);
+      o[2 * i + 1] = pack_code_bf16x2(f2, f3);
     }
   } else {
     // E4M3 code s.eeee.mmm -> BF16 with the sign at bit 15 and eeee.mmm at bits
@@ -1061,7 +1051,7 @@ __global__ void __launch_bounds__(640, 1)
           for (int e = 0; e < 4; ++e) {
             const float lo = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(w[e] & 0xFFFFu), xsc);
             const float hi = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(w[e] >> 16), xsc);
-            o[e] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+            o[e] = pack_code_bf16x2(lo, hi);
           }
           sts128(xb + 16 * c, make_uint4(o[0], o[1], o[2], o[3]));
         }
@@ -1394,7 +1384,7 @@ cudaError_t launch_fp8_gemm(const GemmArgs &g, const DeviceInfo &dev, cudaStream
   if (g.xq) {  // fused quantization: cooperative launch (every CTA resident)
     if (g.x_scale_per_token || !g.xq_flags) return cudaErrorInvalidValue;
     CUtensorMap tx;  // the BF16 activations, chunks of XQ_ROWS rows of a 128 x 128 task tile
-    if (!make_map(&tx, g.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, Fp8CfgT<1>::XQ_ROWS,
+    if (!make_map(&tx, g.xq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.M, g.K, C::BK, Fp8CfgT<1, 1>::XQ_ROWS,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const size_t fb = fp8_xq_flag_bytes(g.M, g.K);

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) k_quantize_act_i8bf16(const uint4 *__rest
     for (int j = 0; j < 4; ++j) {
       const float lo = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(in[j] & 0xFFFFu), s);
       const float hi = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(in[j] >> 16), s);
-      out[j] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+      out[j] = pack_code_bf16x2(lo, hi);
     }
     q[i] = make_uint4(out[0], out[1], out[2], out[3]);
   }
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) k_i8_to_bf16(const uint4 *__restrict__ q,
       for (int h = 0; h < 2; ++h) {
         const float lo = (float)(int8_t)(w[j] >> (16 * h));
         const float hi = (float)(int8_t)(w[j] >> (16 * h + 8));
-        o[2 * j + h] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+        o[2 * j + h] = pack_code_bf16x2(lo, hi);
       }
     }
     out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(256) k_quantize_act_dyn(const uint16_t *__rest
       for (int j = 0; j < 4; ++j) {
         const float lo = (float)(int8_t)quantize_one<QLIN_INT8, true>(bf16_bits_to_f32(w[j] & 0xFFFFu), scl);
         const float hi = (float)(int8_t)quantize_one<QLIN_INT8, true>(bf16_bits_to_f32(w[j] >> 16), scl);
-        o[j] = (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+        o[j] = pack_code_bf16x2(lo, hi);
       }
       reinterpret_cast<uint4 *>((uint16_t *)q + m * K)[i] = make_uint4(o[0], o[1], o[2], o[3]);
     } else {
