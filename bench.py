@@ -180,7 +180,20 @@ class GpuWorkload:
         for l in self.lins:
             wkeys.setdefault((l.workload, l.layer, l.name, l.K, l.N, l.qtype), l)
         self.weight_bytes = sum(l.N * l.K for l in wkeys.values())
-        self.copies = copies if self.weight_bytes < 4 * L2_BYTES else 1
+        # enough alternating weight copies that a pass over them streams at least
+        # twice the L2 for every kernel's calls (at most 16 copies), so neither the
+        # step nor a kernel's isolated graph is served from L2; one copy when the
+        # weights alone exceed that
+        ops = {"w8a16": capi.QLIN_OP_W8A16_LINEAR, "w8a8": capi.QLIN_OP_W8A8_LINEAR,
+               "w8a8dyn": capi.QLIN_OP_W8A8_DYNAMIC_LINEAR}
+        kbytes = {}
+        for l in self.lins:
+            k = capi.qlin_kernel_name(ops[l.form], l.qtype, l.M, l.K, l.N)
+            kbytes[k] = kbytes.get(k, 0) + alg_bytes(l)
+        if self.weight_bytes >= 2 * L2_BYTES:
+            self.copies = 1
+        else:
+            self.copies = min(16, max(copies, -(-2 * L2_BYTES // min(kbytes.values()))))
         self.wsets = [dict() for _ in range(self.copies)]
         self.scales = {}
         # the 36-layer stack draws its tensors with a seeded device generator

@@ -682,10 +682,11 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ, PAIR>::THREADS, 1)
 //                (static per-tensor scale) into integer-valued BF16 before it
 //                releases the block to the MMA, so the linear is one kernel.
 //         I8:    B = activation codes stored as integer-valued BF16; the MMA
-//                accumulates fp32 over chunks of 512 k, where every partial sum
-//                is an integer below 127*127*512 < 2^23 and therefore exact; the
-//                epilogue warps add each chunk into int32 registers, so the full
-//                accumulator is the exact integer sum.  Output: raw int32, or
+//                accumulates fp32 over chunks of 1024 k, where every partial sum
+//                is an integer below 127*127*1024 < 2^24 and therefore exact; the
+//                epilogue warps add each chunk into int32 sums (registers, or
+//                tensor memory for 128-token tiles), so the full accumulator is
+//                the exact integer sum.  Output: raw int32, or
 //                y = acc * (s_x * s_w[n]) + bias[n].
 enum SwapMode { kSwapW8A16 = 0, kSwapI8Scaled = 1, kSwapI8Raw = 2, kSwapI8Fused = 3 };
 
@@ -714,11 +715,17 @@ struct DqCfg {
   // accumulate latency, not its throughput, so consecutive k-blocks rotate
   // over NACC independent accumulator tiles (summed in a fixed order by the
   // epilogue); ND sets of them alternate between consecutive output tiles.
-  static constexpr int NACC = BNT <= 32 ? 4 : BNT <= 128 ? 2 : 1;
+  // INT8 (exact int32 sums) with 128-token tiles: the epilogue's running int32
+  // sums live in tensor memory (SUMCOL..SUMCOL + BNT) instead of registers, one
+  // accumulator per chunk, two alternating.
+  static constexpr bool TSUM = MODE != 0 && BNT > 64;
+  static constexpr int NACC = TSUM ? 1 : BNT <= 32 ? 4 : BNT <= 128 ? 2 : 1;
   static constexpr int ISSUERS = NACC >= 2 ? 2 : 1;  // MMA-issuing threads (own accumulators each)
   static constexpr int DSTRIDE = NACC * BNT;         // columns of one accumulator set
-  static constexpr int ND = 2 * DSTRIDE <= 256 ? 2 : 1;
-  static constexpr int ACOL = ND * DSTRIDE <= 128 ? 128 : 256;  // first TMEM column of the A ring
+  static constexpr int ND = TSUM || 2 * DSTRIDE <= 256 ? 2 : 1;
+  static constexpr int SUMCOL = ND * DSTRIDE;  // TSUM: int32 running sums
+  // first TMEM column of the A ring
+  static constexpr int ACOL = TSUM ? SUMCOL + BNT : ND * DSTRIDE <= 128 ? 128 : 256;
   // Ring depths.  mbarrier.try_wait.parity only tells the current phase from
   // the previous one, so a waiter must never be more than one phase ahead of a
   // slot.  Every waiter below is one of several consumers that take blocks
@@ -726,10 +733,10 @@ struct DqCfg {
   // earlier block, i.e. when the ring depth is a multiple of the number of
   // consumers sharing that ring:
   //   raw ring      (3 converter quads)               R  % 3 == 0
-  //   TMEM A ring   (3 quads wait a_empty, issuers     NA % 6 == 0
+  //   TMEM A ring   (3 quads wait a_empty, issuers     NA % (3 x ISSUERS) == 0
   //                  wait a_full)
   //   activations   (ISSUERS MMA threads)             X  % ISSUERS == 0
-  static constexpr int NA = ACOL == 128 ? 12 : 6;  // A stages, 32 columns (64 BF16 k) each
+  static constexpr int NA = TSUM ? 3 : ACOL == 128 ? 12 : 6;  // A stages, 32 columns (64 BF16 k) each
   //   activations   (fused I8: the 3 quads wait x_full too) X % (QUADS * ISSUERS) == 0
   static constexpr int X = MODE == 3 ? (BNT <= 32 ? 18 : 12) : BNT <= 32 ? 16 : BNT == 64 ? 8 : BNT == 128 ? 8 : 4;
   static constexpr int RING = 200 * 1024;
@@ -842,8 +849,10 @@ __global__ void __launch_bounds__(640, 1)
   using C = DqCfg<BNT, MODE>;
   constexpr bool kI8 = MODE != kSwapW8A16;
   constexpr bool kXQ = MODE == kSwapI8Fused;  // quantize the activation tiles in place
-  constexpr int CH = kI8 ? 8 : (1 << 30);  // k-blocks per exactly accumulated chunk
-  static_assert(!kI8 || BNT <= 64, "int32 sums live in registers");
+  // k-blocks per exactly accumulated chunk: an accumulator takes at most 16 blocks
+  // (1024 products of |q| <= 127), so its sum stays an integer below 2^24
+  constexpr int CH = kI8 ? 16 : (1 << 30);
+  static_assert(!kI8 || BNT <= 64 || C::TSUM, "int32 sums live in registers or in tensor memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *xs = smem + C::X_OFF, *raws = smem + C::RAW_OFF;
@@ -1140,9 +1149,10 @@ __global__ void __launch_bounds__(640, 1)
       const int wrow = !p.glu ? tt * C::BM + nl : (up_row ? p.N + tt * 64 + (nl - 64) : tt * 64 + nl);
       const int ochan = p.glu ? tt * 64 + (nl & 63) : wrow;
       const bool valid = p.glu ? true : wrow < p.N;
-      int32_t sums[kI8 ? BNT : 1];
+      constexpr int NSUM = kI8 && !C::TSUM ? BNT : 1;  // int32 sums held in registers
+      int32_t sums[NSUM];
 #pragma unroll
-      for (int c = 0; c < (kI8 ? BNT : 1); ++c) sums[c] = 0;
+      for (int c = 0; c < NSUM; ++c) sums[c] = 0;
       for (int ch = 0; ch < chunks_per_unit && ok; ++ch, ++cidx) {
         const int db = cidx % C::ND;
         ok = mbar_wait(&acc_full[db], (cidx / C::ND) & 1, abort_flag);
@@ -1200,7 +1210,23 @@ __global__ void __launch_bounds__(640, 1)
             }
           }
         };
-        if constexpr (kI8) {
+        if constexpr (kI8 && C::TSUM) {
+          // the accumulator holds exact integers below 2^23: fold them into the int32
+          // running sums in tensor memory (the first chunk of a tile starts them)
+          const uint32_t ts = tmem + lane_base + C::SUMCOL;
+#pragma unroll 1
+          for (int c = 0; c < BNT; c += 16) {
+            uint32_t r[16], u[16];
+            tmem_ld16(dt + c, r);
+            if (ch > 0) tmem_ld16(ts + c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              u[e] = (uint32_t)((ch > 0 ? (int32_t)u[e] : 0) + __float2int_rn(__uint_as_float(r[e])));
+            tmem_st16(ts + c, u);
+          }
+          tmem_st_wait();
+        } else if constexpr (kI8) {
           // each accumulator holds an exact integer below 2^23: convert, then add in int32
           for (int a = 0; a < nacc; ++a) {
 #pragma unroll
@@ -1261,13 +1287,29 @@ __global__ void __launch_bounds__(640, 1)
         if (lane == 0) mbar_arrive(&acc_empty[db]);
       }
       if constexpr (kI8) {
+        // the tile's int32 sums of tokens c..c+15: from registers, or from tensor memory
+        auto sums16 = [&](int c, int32_t (&s16)[16]) {
+          if constexpr (C::TSUM) {
+            uint32_t u[16];
+            tmem_ld16(tmem + lane_base + C::SUMCOL + c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s16[e] = (int32_t)u[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s16[e] = sums[(c + e) % NSUM];
+          }
+        };
         if (ok) {
           if (S == 1) {
             if constexpr (MODE == kSwapI8Raw) {
-              if (valid) {
 #pragma unroll
-                for (int c = 0; c < BNT; ++c)
-                  if (m0 + c < p.M) ((int32_t *)p.y)[(size_t)(m0 + c) * p.N + wrow] = sums[c];
+              for (int c = 0; c < BNT; c += 16) {  // fully unrolled: sums[] stays in registers
+                int32_t s16[16];
+                sums16(c, s16);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if (valid && m0 + c + e < p.M) ((int32_t *)p.y)[(size_t)(m0 + c + e) * p.N + wrow] = s16[e];
               }
             } else {
               const float sw = valid ? __ldg(p.w_scale + wrow) : 0.0f;
@@ -1276,12 +1318,14 @@ __global__ void __launch_bounds__(640, 1)
 #pragma unroll
               for (int c = 0; c < BNT; c += 16) {  // fully unrolled: sums[] stays in registers
                 if (ok) {
+                  int32_t s16[16];
+                  sums16(c, s16);
                   float v[16];
 #pragma unroll
                   for (int e = 0; e < 16; ++e) {
                     const int m = m0 + c + e;
                     const float sx = p.xs_per_token ? (m < p.M ? __ldg(p.x_scale + m) : 0.0f) : sx0;
-                    v[e] = fmaf((float)sums[c + e], sx * sw, b);
+                    v[e] = fmaf((float)s16[e], sx * sw, b);
                   }
                   ok = emit16(m0, c, ochan, v);
                 }
@@ -1290,7 +1334,12 @@ __global__ void __launch_bounds__(640, 1)
           } else {
             int32_t *red = reinterpret_cast<int32_t *>(smem);
 #pragma unroll
-            for (int c = 0; c < BNT; ++c) red[c * C::BM + nl] = sums[c];
+            for (int c = 0; c < BNT; c += 16) {
+              int32_t s16[16];
+              sums16(c, s16);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) red[(c + e) * C::BM + nl] = s16[e];
+            }
           }
         }
       }
@@ -1463,7 +1512,7 @@ int w8_swap_bnt(int64_t M, int64_t N, int64_t K, int sms) {
   };
   return cost(128, 1.0) < cost(256, 1.63) ? 128 : 256;
 }
-int i8_swap_bnt(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+int i8_swap_bnt(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
 // Split-K factor: CTAs of a cluster that share one output tile when the tiles
 // alone cannot fill the GPU.  Each CTA of a cluster stages a 128 x BNT fp32
@@ -1540,9 +1589,12 @@ cudaError_t launch_i8_swap(const GemmArgs &g, const void *xb, bool raw, const De
     case 32:
       return raw ? launch_dq_t<32, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)
                  : launch_dq_t<32, QLIN_INT8, kSwapI8Scaled>(g, xb, dev, st);
-    default:
+    case 64:
       return raw ? launch_dq_t<64, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)
                  : launch_dq_t<64, QLIN_INT8, kSwapI8Scaled>(g, xb, dev, st);
+    default:
+      return raw ? launch_dq_t<128, QLIN_INT8, kSwapI8Raw>(g, xb, dev, st)
+                 : launch_dq_t<128, QLIN_INT8, kSwapI8Scaled>(g, xb, dev, st);
   }
 }
 

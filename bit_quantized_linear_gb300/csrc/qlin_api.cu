@@ -152,19 +152,19 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
     case QLIN_OP_I8_GEMM_S32: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
-      static const char *names[3] = {"k_i8_to_bf16+k_w8_dq<16,i8>", "k_i8_to_bf16+k_w8_dq<32,i8>",
-                                     "k_i8_to_bf16+k_w8_dq<64,i8>"};
+      static const char *names[4] = {"k_i8_to_bf16+k_w8_dq<16,i8>", "k_i8_to_bf16+k_w8_dq<32,i8>",
+                                     "k_i8_to_bf16+k_w8_dq<64,i8>", "k_i8_to_bf16+k_w8_dq<128,i8>"};
       const int b = i8_swap_bnt(M);
-      return names[b == 16 ? 0 : b == 32 ? 1 : 2];
+      return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : 3];
     }
     case QLIN_OP_W8A8_DYNAMIC_LINEAR: {
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
       if (qtype == QLIN_E4M3) return "k_quantize_act_dyn+k_fp8_gemm";
-      static const char *names[3] = {"k_quantize_act_dyn+k_w8_dq<16,i8>", "k_quantize_act_dyn+k_w8_dq<32,i8>",
-                                     "k_quantize_act_dyn+k_w8_dq<64,i8>"};
+      static const char *names[4] = {"k_quantize_act_dyn+k_w8_dq<16,i8>", "k_quantize_act_dyn+k_w8_dq<32,i8>",
+                                     "k_quantize_act_dyn+k_w8_dq<64,i8>", "k_quantize_act_dyn+k_w8_dq<128,i8>"};
       const int b = i8_swap_bnt(M);
-      return names[b == 16 ? 0 : b == 32 ? 1 : 2];
+      return names[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : 3];
     }
     case QLIN_OP_KV_STORE_MIXED:
     case QLIN_OP_KV_LOAD_MIXED: {
@@ -182,12 +182,13 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
       if (qtype == QLIN_E4M3) return fp8_xq_used(M, K, N, sm_count()) ? "k_fp8_gemm<xq>" : "k_quantize_act+k_fp8_gemm";
-      static const char *names[3] = {"k_quantize_act_i8bf16+k_w8_dq<16,i8>",
+      static const char *names[4] = {"k_quantize_act_i8bf16+k_w8_dq<16,i8>",
                                      "k_quantize_act_i8bf16+k_w8_dq<32,i8>",
-                                     "k_quantize_act_i8bf16+k_w8_dq<64,i8>"};
-      static const char *fused[3] = {"k_w8_dq<16,i8,xq>", "k_w8_dq<32,i8,xq>", "k_w8_dq<64,i8,xq>"};
+                                     "k_quantize_act_i8bf16+k_w8_dq<64,i8>",
+                                     "k_quantize_act_i8bf16+k_w8_dq<128,i8>"};
+      static const char *fused[4] = {"k_w8_dq<16,i8,xq>", "k_w8_dq<32,i8,xq>", "k_w8_dq<64,i8,xq>", "invalid"};
       const int b = i8_swap_bnt(M);
-      return (i8_fused_quant(M) ? fused : names)[b == 16 ? 0 : b == 32 ? 1 : 2];
+      return (i8_fused_quant(M) ? fused : names)[b == 16 ? 0 : b == 32 ? 1 : b == 64 ? 2 : 3];
     }
   }
   return "invalid";

@@ -265,11 +265,11 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
       int i = 0;
       for (; i < nkb; ++i) {
         const int s = i % NS;
-        if (i >= NS) {
-          if (!mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
-            *abort_flag = 1;
-            break;
-          }
+        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) & 1) ^ 1, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (i >= pre) {  // stages past the ones armed before the wait
           mbar_arrive_expect_tx(&full[s], C::STAGE);
           load_w(i);
         }

@@ -37,7 +37,7 @@ QT = {"int8": oracle.INT8, "e4m3": oracle.E4M3}
 # call orders: the largest call first, so the smaller ones after it run over
 # bytes it left in the scratch
 ORDERS = {
-    "int8": [(300, 2048, 272, "k_quantize_act_i8bf16+k_w8_dq<64,i8>"),
+    "int8": [(300, 2048, 272, "k_quantize_act_i8bf16+k_w8_dq<128,i8>"),
              (40, 1024, 384, "k_w8_dq<64,i8,xq>"),
              (7, 2048, 512, "k_w8_dq<16,i8,xq>")],
     "e4m3": [(8192, 4096, 2048, "k_fp8_gemm<xq>"),
