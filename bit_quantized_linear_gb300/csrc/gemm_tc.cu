@@ -530,34 +530,43 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ, PAIR>::THREADS, 1)
       }
       ++emitted;
     };
-    // Column factors of 8 channels from n (the same for every lane: broadcast
-    // loads): scale s_x * s_w[n + i] and bias; zero from channel `end` on (n is a
-    // multiple of 8 and end of 16, so the 8 are all inside or all outside).  end
-    // is N, or 2N for the up channels of the merged gate_up weight.
-    auto col_factors = [&](int n, int end, float (&sc)[8], float (&bi)[8]) {
-      if (n < end) {
-        const float4 *w4 = reinterpret_cast<const float4 *>(p.w_scale + n);
-        const float4 v0 = __ldg(w4), v1 = __ldg(w4 + 1);
-        sc[0] = sx * v0.x, sc[1] = sx * v0.y, sc[2] = sx * v0.z, sc[3] = sx * v0.w;
-        sc[4] = sx * v1.x, sc[5] = sx * v1.y, sc[6] = sx * v1.z, sc[7] = sx * v1.w;
-        if (p.bias) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.bias + n));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) bi[2 * e] = bf16_bits_to_f32(w[e] & 0xFFFFu), bi[2 * e + 1] = bf16_bits_to_f32(w[e] >> 16);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) bi[i] = 0.0f;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sc[i] = 0.0f, bi[i] = 0.0f;
+    // Column factors of this warp's 128 columns of a tile, one float4 per lane:
+    // s_x * s_w[n] and the bias, zero from channel `end` on (n is a multiple of 4
+    // and end of 16, so a lane's 4 are all inside or all outside).  Plain: lane l
+    // holds the tile's columns 128 half + 4l..; glu: lanes 0..15 the gate
+    // channels 64 half + 4l.. (end N), lanes 16..31 their up channels N further
+    // on (end 2N).  They are loaded before the wait for the tile's accumulator,
+    // so their latency hides behind the MMAs; a column's factor is then one
+    // shuffle from the lane that holds it.
+    auto load_factors = [&](int n0, float4 &fs, float4 &fb) {
+      int n = n0 + 128 * half + 4 * lane, end = p.N;
+      if (p.glu) {
+        const int g = n0 / 2 + 64 * half + 4 * (lane & 15);
+        n = lane < 16 ? g : p.N + g;
+        end = lane < 16 ? p.N : 2 * p.N;
       }
+      fs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      fb = fs;
+      if (n < end) {
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(p.w_scale + n));
+        fs = make_float4(sx * w.x, sx * w.y, sx * w.z, sx * w.w);
+        if (p.bias) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p.bias + n));
+          fb = make_float4(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16), bf16_bits_to_f32(v.y & 0xFFFFu),
+                           bf16_bits_to_f32(v.y >> 16));
+        }
+      }
+    };
+    // component k (0..3, known at compile time) of lane src's float4, to every lane
+    auto shfl4 = [&](const float4 &f, int k, int src) {
+      return __shfl_sync(0xffffffffu, k == 0 ? f.x : k == 1 ? f.y : k == 2 ? f.z : f.w, src);
     };
     bool ok = true;
     for (int j = 0; j < my_tiles && ok; ++j) {
       const int t = cid + j * G, b = j & 1;
       const int m0 = tile_m0(t), n0 = tile_n0(t);
+      float4 fs, fb;
+      load_factors(n0, fs, fb);
       ok = mbar_wait(&acc_full[b], (j >> 1) & 1, abort_flag);
       tc_fence_after();
       // tcgen05.ld is warp-collective: every lane of the warp takes the same path
@@ -594,18 +603,18 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ, PAIR>::THREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              // gate channels nb + 16q + 8hh.., and the up channels N further on (N % 16 == 0)
-              float sg[8], bg[8], su[8], bu[8];
-              col_factors(nb + 16 * q + 8 * hh, p.N, sg, bg);
-              col_factors(p.N + nb + 16 * q + 8 * hh, 2 * p.N, su, bu);
+              // gate channels nb + 16q + 8hh.. (this warp's gate column jg..), and the
+              // up channels N further on, held by lanes 16..31
+              const int jg = (c - 64 * half) + 16 * q + 8 * hh;
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
                 float v[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                  const int i = 2 * h + e, col = 8 * hh + i;
-                  const float g = fmaf(__uint_as_float(rg[col]), sxm * sg[i], bg[i]);
-                  const float u = fmaf(__uint_as_float(ru[col]), sxm * su[i], bu[i]);
+                  const int i = 2 * h + e, col = 8 * hh + i, src = (jg + i) >> 2;
+                  const float g = fmaf(__uint_as_float(rg[col]), sxm * shfl4(fs, i & 3, src), shfl4(fb, i & 3, src));
+                  const float u =
+                      fmaf(__uint_as_float(ru[col]), sxm * shfl4(fs, i & 3, 16 + src), shfl4(fb, i & 3, 16 + src));
                   v[e] = silu_f(g) * u;
                 }
                 o[8 * q + 4 * hh + h] = pack_bf16x2(v[0], v[1]);
@@ -624,13 +633,13 @@ __global__ void __launch_bounds__(Fp8CfgT<XQ, PAIR>::THREADS, 1)
           uint32_t o[16];
 #pragma unroll
           for (int hh = 0; hh < 4; ++hh) {
-            float sc[8], bi[8];
-            col_factors(nb + 8 * hh, p.N, sc, bi);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const int i = 2 * h, col = 8 * hh + i;
-              o[4 * hh + h] = pack_bf16x2(fmaf(__uint_as_float(r[col]), sxm * sc[i], bi[i]),
-                                          fmaf(__uint_as_float(r[col + 1]), sxm * sc[i + 1], bi[i + 1]));
+              // this warp's columns j, j + 1 (j even): factors from lane j / 4
+              const int i = 2 * h, col = 8 * hh + i, j = (c - 128 * half) + col, src = j >> 2;
+              o[4 * hh + h] = pack_bf16x2(
+                  fmaf(__uint_as_float(r[col]), sxm * shfl4(fs, i & 3, src), shfl4(fb, i & 3, src)),
+                  fmaf(__uint_as_float(r[col + 1]), sxm * shfl4(fs, (i + 1) & 3, src), shfl4(fb, (i + 1) & 3, src)));
             }
           }
           if (nb < p.N) emit(o, nb, yrow0);
