@@ -390,6 +390,9 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"

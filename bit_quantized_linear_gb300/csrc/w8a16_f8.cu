@@ -51,7 +51,9 @@ using namespace tc;
 namespace {
 
 // ------------------------------------------------------------ activation split
-constexpr int kSplitThreads = 256, kSplitChunk = 8 * kSplitThreads, kSplitMaxLoads = 16;
+// A token row is split by one cluster of at most kSplitMaxChunks CTAs, each over
+// its own chunk of at most kSplitMaxPer 16-byte pieces per thread.
+constexpr int kSplitThreads = 256, kSplitMaxChunks = 8, kSplitMaxPer = 8;
 constexpr int kSplitTerms = 4;  // x1, x2 (band A) and x3, x4 (band B)
 
 // Least power of two s with 448 s >= a (a > 0), from the exponent bits alone:
@@ -96,16 +98,27 @@ __device__ __forceinline__ void split_pair(uint32_t word, float r, uint32_t (&c)
   c[0] = (uint32_t)h1 & a, c[1] = (uint32_t)h2 & a, c[2] = (uint32_t)h1 & b, c[3] = (uint32_t)h2 & b;
 }
 
-// Token row m, chunk c of kSplitChunk elements: one CTA.  Every CTA of a row
-// reads the whole row for its abs-max (the row is small and L2-resident; all of
-// a thread's loads are issued before any is used) and keeps its own chunk in
-// registers, then writes that chunk's four E4M3 terms into the B-operand
-// layout: token tile j (tt tokens) owns rows [4 tt j, 4 tt j + 4 tt) of xs,
-// the x1 rows of its tokens first, then x2, x3 and x4.
+// Token row m: one cluster of gridDim.x CTAs, CTA c over pieces [c P, c P + P)
+// of the row (P = `per` 16-byte pieces of 8 elements; each thread holds up to
+// kSplitMaxPer of them in registers).  Each CTA takes the abs-max of its own
+// chunk and stores it into every CTA of the cluster (distributed shared
+// memory); after one cluster barrier each CTA has the row's maximum, so the
+// row is read once in all.  Each CTA then writes its chunk's four E4M3 terms
+// into the B-operand layout: token tile j (tt tokens) owns rows
+// [4 tt j, 4 tt j + 4 tt) of xs, the x1 rows of its tokens first, then x2, x3
+// and x4.
 __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *__restrict__ x, int M, int K,
-                                                               int tt, uint8_t *__restrict__ xs,
-                                                               float *__restrict__ xscale) {
+                                                               int tt, int per, uint8_t *__restrict__ xs,
+                                                               float *__restrict__ xscale, unsigned *status) {
   __shared__ float wmax[kSplitThreads / 32];
+  __shared__ float cmax[kSplitMaxChunks];  // every chunk's maximum, stored by its CTA
+  // the chunks exchange their maxima through the cluster's shared memory: without
+  // that cluster shape, report and leave before anything is read or written
+  const int C = gridDim.x, c = blockIdx.x;
+  if ((int)cluster_nctarank() != C) {
+    if (threadIdx.x == 0 && c == 0) set_status(status, QLIN_ERR_UNSUPPORTED);
+    return;
+  }
   // The FP8 linear that follows may start at once: before its own wait for this
   // kernel it only arms barriers and loads weight tiles, so its CTAs take the
   // SMs that the previous linear frees during its tail.  Nothing here is
@@ -114,43 +127,46 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
   pdl_wait();
   const int m = blockIdx.y, n8 = K / 8;  // K % 16 == 0
   const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
-  const int mine = blockIdx.x * kSplitThreads + threadIdx.x;  // this thread's 8 elements of the chunk
-  uint4 own = make_uint4(0, 0, 0, 0);
+  const int u0 = c * per, u1 = min(n8, u0 + per);
+  uint4 v[kSplitMaxPer];
   float a = 0.0f;
-  // the whole row, kSplitMaxLoads 16-byte loads in flight per thread at a time
-  for (int base = threadIdx.x; base < n8; base += kSplitThreads * kSplitMaxLoads) {
-    uint4 v[kSplitMaxLoads];
 #pragma unroll
-    for (int u = 0; u < kSplitMaxLoads; ++u) {
-      const int i = base + u * kSplitThreads;
-      v[u] = i < n8 ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < kSplitMaxLoads; ++u) {
-      a = fmaxf(a, absmax8(v[u]));
-      if (base + u * kSplitThreads == mine) own = v[u];
-    }
+  for (int i = 0; i < kSplitMaxPer; ++i) {  // all of this thread's loads in flight at once
+    const int u = u0 + (int)threadIdx.x + i * kSplitThreads;
+    v[i] = u < u1 ? __ldg(row + u) : make_uint4(0, 0, 0, 0);
   }
+#pragma unroll
+  for (int i = 0; i < kSplitMaxPer; ++i) a = fmaxf(a, absmax8(v[i]));
   a = warp_max(a);
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = a;
   __syncthreads();
-  a = wmax[0];
+  if (threadIdx.x < C) {  // this chunk's maximum into CTA threadIdx.x of the cluster
+    float cm = wmax[0];
 #pragma unroll
-  for (int w = 1; w < kSplitThreads / 32; ++w) a = fmaxf(a, wmax[w]);
+    for (int w = 1; w < kSplitThreads / 32; ++w) cm = fmaxf(cm, wmax[w]);
+    st_dsmem_f32(map_peer_smem(smem_u32(&cmax[c]), threadIdx.x), cm);
+  }
+  cluster_sync();  // every chunk's maximum has arrived
+  a = cmax[0];
+  for (int q = 1; q < C; ++q) a = fmaxf(a, cmax[q]);
   const float s = split_scale(a), r = 1.0f / s;  // powers of two: exact
-  if (blockIdx.x == 0 && threadIdx.x == 0) xscale[m] = s;
-  if (mine >= n8) return;
+  if (c == 0 && threadIdx.x == 0) xscale[m] = s;
   const int j = m / tt, t = m % tt;
   uint8_t *x1 = xs + ((size_t)kSplitTerms * tt * j + t) * K;
   const size_t term = (size_t)tt * K;  // x2, x3, x4 follow, tt rows apart
-  const uint32_t w[4] = {own.x, own.y, own.z, own.w};
-  uint32_t c[4][kSplitTerms];  // codes of the four words' terms, two per 16 bits
 #pragma unroll
-  for (int e = 0; e < 4; ++e) split_pair(w[e], r, c[e]);
+  for (int i = 0; i < kSplitMaxPer; ++i) {
+    const int u = u0 + (int)threadIdx.x + i * kSplitThreads;
+    if (u >= u1) break;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t cw[4][kSplitTerms];  // codes of the four words' terms, two per 16 bits
 #pragma unroll
-  for (int q = 0; q < kSplitTerms; ++q)
-    *reinterpret_cast<uint2 *>(x1 + q * term + 8 * mine) =
-        make_uint2(c[0][q] | (c[1][q] << 16), c[2][q] | (c[3][q] << 16));
+    for (int e = 0; e < 4; ++e) split_pair(w[e], r, cw[e]);
+#pragma unroll
+    for (int q = 0; q < kSplitTerms; ++q)
+      *reinterpret_cast<uint2 *>(x1 + q * term + 8 * (size_t)u) =
+          make_uint2(cw[0][q] | (cw[1][q] << 16), cw[2][q] | (cw[3][q] << 16));
+  }
 }
 
 // ------------------------------------------------------------ the FP8 linear
@@ -438,9 +454,15 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
   if (!map_u8(&tw, g.qw, g.glu ? 2 * g.N : g.N, g.K, g.glu ? 64 : 128) ||
       !map_u8(&tx, xs, (int64_t)ttiles * C::NB, g.K, C::NB))
     return cudaErrorInvalidValue;
-  const int chunks = (int)((g.K + kSplitChunk - 1) / kSplitChunk);
-  cudaError_t e = launch_kernel(k_w8a16_split, dim3((unsigned)chunks, (unsigned)g.M), dim3(kSplitThreads), 0, st, 1,
-                                (const uint16_t *)g.a, (int)g.M, (int)g.K, TT, xs, xscale);
+  // one cluster per token row: C CTAs of at most kSplitMaxPer 16-byte pieces per thread
+  const int n8 = (int)(g.K / 8);
+  int chunks = (n8 + kSplitThreads - 1) / kSplitThreads;
+  if (chunks > kSplitMaxChunks) chunks = kSplitMaxChunks;
+  const int per = (n8 + chunks - 1) / chunks;
+  if (per > kSplitMaxPer * kSplitThreads) return cudaErrorInvalidValue;  // K beyond 2^17 (refused on the host)
+  cudaError_t e = launch_kernel_x(k_w8a16_split, dim3((unsigned)chunks, (unsigned)g.M), dim3(kSplitThreads), 0, st,
+                                  (unsigned)chunks, (const uint16_t *)g.a, (int)g.M, (int)g.K, TT, per, xs, xscale,
+                                  dev.status);
   if (e != cudaSuccess) return e;
   W8F8Params p;
   p.M = (int)g.M;
