@@ -143,7 +143,7 @@ const char *qlin_kernel_name(qlin_op op, qlin_qtype qtype, int64_t M, int64_t K,
       if (check_linear_shape(M, K, N)) return "invalid";
       if (M == 0) return "none";
       if (qtype == QLIN_E4M3 && M <= kW8A16F8MaxM) {
-        return w8a16_f8_tt(M) == 16 ? "k_w8a16_split+k_w8a16_f8<16>" : "k_w8a16_split+k_w8a16_f8<32>";
+        return w8a16_f8_tt(M) <= 16 ? "k_w8a16_split+k_w8a16_f8<16>" : "k_w8a16_split+k_w8a16_f8<32>";
       }
       static const char *names[5] = {"k_w8_dq<16>", "k_w8_dq<32>", "k_w8_dq<64>", "k_w8_dq<128>", "k_w8_dq<256>"};
       const int b = w8_swap_bnt(M, N, K, sm_count());

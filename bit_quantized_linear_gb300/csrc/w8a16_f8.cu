@@ -181,28 +181,33 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
 // k_w8a16_split through the workspace, with one power-of-two scale per token
 // row; the epilogue folds that scale into the partial tile, so the cluster's
 // sum of the partials needs no per-token factor.
-template <int TT>
+// The token tile tt (4, 8 or 16 up to TMAX = 16; 32 for TMAX = 32) is chosen
+// at run time: the fewer the tokens, the smaller each stage's B tile, so the
+// deeper the ring and the more weight tiles stream in before the wait for the
+// split.
+template <int TMAX>
 struct W8F8Cfg {
-  static constexpr int BM = 128, BK = 128, NB = kSplitTerms * TT;
-  static constexpr int A_BYTES = BM * BK, B_BYTES = NB * BK;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  // The ring depth is a launch parameter (stages of STAGE bytes); the barriers
-  // follow the ring.
-  static constexpr int MAX_STAGES = 14, BAR_BYTES = 256;
-  static constexpr int PART_BYTES = TT * BM * 4;  // [TT tokens][BM rows] fp32, in the drained ring
+  static constexpr int BM = 128, BK = 128, NB_MAX = kSplitTerms * TMAX;
+  static constexpr int A_BYTES = BM * BK;
+  static __host__ __device__ constexpr int stage_bytes(int tt) { return A_BYTES + kSplitTerms * tt * BK; }
+  // The ring depth is a launch parameter; the barriers follow the ring, then
+  // the tile's per-row weight scales and biases and the per-token scales.
+  static constexpr int MAX_STAGES = 14, BAR_BYTES = 256, AUX_BYTES = (2 * BM + 32) * 4;
   static constexpr int THREADS = 192;
-  static constexpr uint32_t TMEM_COLS = NB;  // 64 or 128, a power of two
-  static constexpr uint32_t IDESC = umma_idesc(0, 0, BM, NB);
-  static constexpr int smem_bytes(int stages) { return stages * STAGE + BAR_BYTES + 1024; }
-  static_assert(PART_BYTES <= 2 * STAGE, "partial tile in a ring of two or more stages");
+  static constexpr uint32_t TMEM_COLS = NB_MAX;  // 64 or 128, a power of two
+  static constexpr int smem_bytes(int tt, int stages) {
+    return stages * stage_bytes(tt) + BAR_BYTES + AUX_BYTES + 1024;
+  }
+  static_assert(TMAX == 16 || TMAX == 32, "token tile bound");
   static_assert((2 * MAX_STAGES + 1) * 8 + 8 <= BAR_BYTES, "barriers");
-  static_assert(STAGE % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
+  static_assert(stage_bytes(4) % 1024 == 0, "stage alignment (128-byte swizzle atoms)");
 };
 
 struct W8F8Params {
   int M, N, K;  // N: output channels (I for the merged gate_up)
   int glu;
   int ntiles, splits, stages;
+  int tt;  // tokens per tile
   const float *w_scale;
   const float *x_scale;  // per token, from the split
   const uint16_t *bias;
@@ -214,16 +219,17 @@ __device__ __forceinline__ uint8_t *align1k(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
 
-template <int TT>
-__global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
+template <int TMAX>
+__global__ void __launch_bounds__(W8F8Cfg<TMAX>::THREADS, 1)
     k_w8a16_f8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, W8F8Params p) {
-  using C = W8F8Cfg<TT>;
+  using C = W8F8Cfg<TMAX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1k(smem_raw);
-  const int NS = p.stages;
-  uint64_t *full = (uint64_t *)(smem + NS * C::STAGE), *empty = full + NS, *acc_full = empty + NS;
+  const int NS = p.stages, tt = p.tt, NB = kSplitTerms * tt, STAGE = C::stage_bytes(tt);
+  uint64_t *full = (uint64_t *)(smem + NS * STAGE), *empty = full + NS, *acc_full = empty + NS;
   uint32_t *tmem_slot = (uint32_t *)(acc_full + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+  float *rsc = (float *)(smem + NS * STAGE + C::BAR_BYTES), *rbi = rsc + C::BM, *xsc = rbi + C::BM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.splits;
   // the K splits of a tile reduce through their cluster's shared memory: without
@@ -256,7 +262,7 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   if (warp == 0) {  // ------------------------------- TMA producer
     if (lane == 0) {
       auto load_w = [&](int i) {
-        uint8_t *st = smem + (i % NS) * C::STAGE;
+        uint8_t *st = smem + (i % NS) * STAGE;
         const int k = (kb0 + i) * C::BK;
         if (p.glu) {  // 64 gate rows, then their 64 up rows
           tma_load_2d(&tm_w, &full[i % NS], st, k, tile * 64);
@@ -266,15 +272,15 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
         }
       };
       auto load_x = [&](int i) {
-        tma_load_2d(&tm_x, &full[i % NS], smem + (i % NS) * C::STAGE + C::A_BYTES, (kb0 + i) * C::BK, tj * C::NB);
+        tma_load_2d(&tm_x, &full[i % NS], smem + (i % NS) * STAGE + C::A_BYTES, (kb0 + i) * C::BK, tj * NB);
       };
       // The weight tiles of the first stages are loaded before the wait for the
-      // previous kernel: weight codes are never written by a kernel that lets
-      // this one start early (the weight quantizer lets no later kernel start
-      // before it completes).  The activation terms follow the wait.
+      // previous kernel: weights are never written by a kernel that lets this
+      // one start early (the weight quantizer lets no later kernel start before
+      // it completes).  The activation terms follow the wait.
       const int pre = nkb < NS ? nkb : NS;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], C::STAGE);
+        mbar_arrive_expect_tx(&full[i], STAGE);
         load_w(i);
       }
       pdl_wait();
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
           break;
         }
         if (i >= pre) {  // stages past the ones armed before the wait
-          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          mbar_arrive_expect_tx(&full[s], STAGE);
           load_w(i);
         }
         load_x(i);
@@ -295,6 +301,7 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
     }
   } else if (warp == 1) {  // ------------------------ MMA issuer
     if (lane == 0) {
+      const uint32_t idesc = umma_idesc(0, 0, C::BM, NB);
       bool ok = true;
       int i = 0;
       for (; i < nkb; ++i) {
@@ -304,11 +311,11 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a = smem_u32(smem + s * C::STAGE);
+        const uint32_t a = smem_u32(smem + s * STAGE);
         const uint64_t ad = umma_desc_sw128(a), bd = umma_desc_sw128(a + C::A_BYTES);
 #pragma unroll
         for (int j = 0; j < 4; ++j)  // K = 32 codes per instruction
-          mma_fp8(tmem, ad + 2 * j, bd + 2 * j, C::IDESC, (i > 0 || j > 0) ? 1u : 0u);
+          mma_fp8(tmem, ad + 2 * j, bd + 2 * j, idesc, (i > 0 || j > 0) ? 1u : 0u);
         mma_commit(&empty[s]);
       }
       if (ok) mma_commit(acc_full);
@@ -319,28 +326,37 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   } else {  // ------------------------------------- epilogue: accumulators -> partial tile
     const int q4 = warp & 3, r = q4 * 32 + lane;  // TMEM lane = weight row of the tile
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    // While the main loop runs: this row's weight scale and bias (weights, so
+    // readable before the wait), then, after it, the tile's token scales.
+    {
+      const int ch = p.glu ? (r < 64 ? tile * 64 + r : p.N + tile * 64 + (r - 64)) : tile * C::BM + r;
+      const bool live = p.glu || ch < p.N;
+      rsc[r] = live ? __ldg(p.w_scale + ch) : 0.0f;
+      rbi[r] = live && p.bias ? bf16_bits_to_f32(__ldg(p.bias + ch)) : 0.0f;
+    }
     bool ok = true;
     pdl_wait();  // the split's scales are complete from here on
-    const int m0 = tj * TT;
+    const int m0 = tj * tt, e = threadIdx.x - 64;
+    if (e < tt) xsc[e] = m0 + e < p.M ? __ldg(p.x_scale + m0 + e) : 0.0f;
+    bar_sync_named(1, 128);  // the four epilogue warps
     ok = ok && mbar_wait(acc_full, 0, abort_flag);
     tc_fence_after();
     if (__all_sync(0xffffffffu, ok && !*abort_flag)) {  // tcgen05.ld is warp-collective
       float *part = reinterpret_cast<float *>(smem);   // the ring is drained: every MMA has read it
 #pragma unroll 1
-      for (int c = 0; c < TT; c += 16) {
-        uint32_t a1[16], a2[16], a3[16], a4[16];  // x1..x4 products of tokens c..c+15
+      for (int c = 0; c < tt; c += 16) {
+        uint32_t a1[16], a2[16], a3[16], a4[16];  // x1..x4 products of tokens c..c+15 (c..tt-1 used)
         tmem_ld16(tmem + lane_base + c, a1);
-        tmem_ld16(tmem + lane_base + TT + c, a2);
-        tmem_ld16(tmem + lane_base + 2 * TT + c, a3);
-        tmem_ld16(tmem + lane_base + 3 * TT + c, a4);
+        tmem_ld16(tmem + lane_base + tt + c, a2);
+        tmem_ld16(tmem + lane_base + 2 * tt + c, a3);
+        tmem_ld16(tmem + lane_base + 3 * tt + c, a4);
         tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          const int m = m0 + c + t;
-          const float sx = m < p.M ? __ldg(p.x_scale + m) : 0.0f;  // the token row's scale
+          if (c + t >= tt) break;
           const float band_a = fmaf(__uint_as_float(a2[t]), 0.0625f, __uint_as_float(a1[t]));
           const float band_b = fmaf(__uint_as_float(a4[t]), 0.0625f, __uint_as_float(a3[t]));
-          part[(c + t) * C::BM + r] = sx * fmaf(band_b, 6.103515625e-05f, band_a);  // 2^-14
+          part[(c + t) * C::BM + r] = xsc[c + t] * fmaf(band_b, 6.103515625e-05f, band_a);  // 2^-14
         }
       }
     } else {
@@ -359,53 +375,50 @@ __global__ void __launch_bounds__(W8F8Cfg<TT>::THREADS, 1)
   // items of one token, so the stores are coalesced
   pdl_wait();  // y belongs to the previous kernels from here on
   {
-    const int rows = p.glu ? 64 : C::BM, R4 = rows / 4, E = TT * R4;
+    const int rows = p.glu ? 64 : C::BM, R4 = rows / 4, E = tt * R4;
     const int e0 = split * E / S, e1 = (split + 1) * E / S;
     const uint32_t pbase = smem_u32(smem);
     auto sum4 = [&](int t, int row) {
-      const uint32_t a = pbase + 4u * (uint32_t)(t * C::BM + row);
-      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (S == 1) return *reinterpret_cast<const float4 *>(smem + 4 * (t * C::BM + row));
-      for (int q = 0; q < S; ++q) {  // fixed order
-        const uint4 u = ld_dsmem_v4(map_peer_smem(a, (uint32_t)q));
-        v.x += __uint_as_float(u.x), v.y += __uint_as_float(u.y), v.z += __uint_as_float(u.z),
-            v.w += __uint_as_float(u.w);
-      }
+      const uint32_t a = pbase + 4u * (uint32_t)(t * C::BM + row);
+      uint4 u[8];  // every peer's piece in flight at once, then the sum in rank order
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < S) u[q] = ld_dsmem_v4(map_peer_smem(a, (uint32_t)q));
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < S)
+          v.x += __uint_as_float(u[q].x), v.y += __uint_as_float(u[q].y), v.z += __uint_as_float(u[q].z),
+              v.w += __uint_as_float(u[q].w);
       return v;
     };
     for (int e = e0 + (int)threadIdx.x; e < e1; e += C::THREADS) {
-      const int t = e / R4, rr = (e - t * R4) * 4, m = tj * TT + t;
+      const int t = e / R4, rr = (e - t * R4) * 4, m = tj * tt + t;
       if (m >= p.M) continue;
+      float o[4];
+      int n;
       if (p.glu) {
-        const int n = tile * 64 + rr;
+        n = tile * 64 + rr;
         const float4 g4 = sum4(t, rr), u4 = sum4(t, 64 + rr);
         const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, us[4] = {u4.x, u4.y, u4.z, u4.w};
-        float o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + n + i)) : 0.0f;
-          const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + n + i)) : 0.0f;
-          const float g = fmaf(gs[i], __ldg(p.w_scale + n + i), bg);
-          const float u = fmaf(us[i], __ldg(p.w_scale + p.N + n + i), bu);
+          const float g = fmaf(gs[i], rsc[rr + i], rbi[rr + i]);
+          const float u = fmaf(us[i], rsc[64 + rr + i], rbi[64 + rr + i]);
           o[i] = silu_f(g) * u;
         }
-        *reinterpret_cast<uint2 *>(p.y + (size_t)m * p.N + n) =
-            make_uint2(f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
-                       f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
       } else {
-        const int n = tile * C::BM + rr;
+        n = tile * C::BM + rr;
         if (n >= p.N) continue;  // N % 16 == 0: the four channels are all in or all out
         const float4 v4 = sum4(t, rr);
         const float vs[4] = {v4.x, v4.y, v4.z, v4.w};
-        const float4 ws = __ldg(reinterpret_cast<const float4 *>(p.w_scale + n));
-        const float sw[4] = {ws.x, ws.y, ws.z, ws.w};
-        float o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = fmaf(vs[i], sw[i], p.bias ? bf16_bits_to_f32(__ldg(p.bias + n + i)) : 0.0f);
-        *reinterpret_cast<uint2 *>(p.y + (size_t)m * p.N + n) =
-            make_uint2(f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
-                       f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
+        for (int i = 0; i < 4; ++i) o[i] = fmaf(vs[i], rsc[rr + i], rbi[rr + i]);
       }
+      *reinterpret_cast<uint2 *>(p.y + (size_t)m * p.N + n) =
+          make_uint2(f32_to_bf16_bits(o[0]) | ((uint32_t)f32_to_bf16_bits(o[1]) << 16),
+                     f32_to_bf16_bits(o[2]) | ((uint32_t)f32_to_bf16_bits(o[3]) << 16));
     }
   }
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, QLIN_ERR_TIMEOUT);
@@ -446,13 +459,14 @@ bool map_u8(CUtensorMap *tm, const void *base, int64_t rows, int64_t cols, uint3
 // Shared memory of one CTA when two share an SM (228 KB, 1 KB of it reserved per CTA).
 constexpr int kCtaSmem = 113 * 1024;
 
-template <int TT>
-cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const DeviceInfo &dev, cudaStream_t st) {
-  using C = W8F8Cfg<TT>;
-  const int ttiles = (int)((g.M + TT - 1) / TT);
+template <int TMAX>
+cudaError_t launch_tt(const GemmArgs &g, int tt, uint8_t *xs, float *xscale, const DeviceInfo &dev,
+                      cudaStream_t st) {
+  using C = W8F8Cfg<TMAX>;
+  const int ttiles = (int)((g.M + tt - 1) / tt), NB = kSplitTerms * tt;
   CUtensorMap tw, tx;
   if (!map_u8(&tw, g.qw, g.glu ? 2 * g.N : g.N, g.K, g.glu ? 64 : 128) ||
-      !map_u8(&tx, xs, (int64_t)ttiles * C::NB, g.K, C::NB))
+      !map_u8(&tx, xs, (int64_t)ttiles * NB, g.K, NB))
     return cudaErrorInvalidValue;
   // one cluster per token row: C CTAs of at most kSplitMaxPer 16-byte pieces per thread
   const int n8 = (int)(g.K / 8);
@@ -461,7 +475,7 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
   const int per = (n8 + chunks - 1) / chunks;
   if (per > kSplitMaxPer * kSplitThreads) return cudaErrorInvalidValue;  // K beyond 2^17 (refused on the host)
   cudaError_t e = launch_kernel_x(k_w8a16_split, dim3((unsigned)chunks, (unsigned)g.M), dim3(kSplitThreads), 0, st,
-                                  (unsigned)chunks, (const uint16_t *)g.a, (int)g.M, (int)g.K, TT, per, xs, xscale,
+                                  (unsigned)chunks, (const uint16_t *)g.a, (int)g.M, (int)g.K, tt, per, xs, xscale,
                                   dev.status);
   if (e != cudaSuccess) return e;
   W8F8Params p;
@@ -469,33 +483,34 @@ cudaError_t launch_tt(const GemmArgs &g, uint8_t *xs, float *xscale, const Devic
   p.N = (int)g.N;
   p.K = (int)g.K;
   p.glu = g.glu;
+  p.tt = tt;
   p.ntiles = g.glu ? (int)(g.N / 64) : (int)((g.N + C::BM - 1) / C::BM);
   const int units = p.ntiles * ttiles, KB = (int)((g.K + C::BK - 1) / C::BK);
   p.splits = w8a16_f8_splits(units, KB, dev.sms);
-  // two CTAs to an SM: as many stages as fit beside the barriers
-  constexpr int fit = (kCtaSmem - C::smem_bytes(0)) / C::STAGE;
-  constexpr int max_stages = fit < C::MAX_STAGES ? fit : C::MAX_STAGES;
-  static_assert(max_stages >= 3, "ring depth");
-  p.stages = max_stages;
+  // two CTAs to an SM: as many stages as fit beside the barriers and scales
+  int stages = (kCtaSmem - C::smem_bytes(tt, 0)) / C::stage_bytes(tt);
+  if (stages > C::MAX_STAGES) stages = C::MAX_STAGES;
+  if (stages < 3) return cudaErrorInvalidValue;
+  p.stages = stages;
   p.w_scale = g.w_scale;
   p.x_scale = xscale;
   p.bias = g.bias;
   p.y = (uint16_t *)g.y;
   p.status = dev.status;
-  static_assert(C::smem_bytes(max_stages) <= kCtaSmem, "shared memory");
   static const cudaError_t attr =
-      cudaFuncSetAttribute(k_w8a16_f8<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes(max_stages));
+      cudaFuncSetAttribute(k_w8a16_f8<TMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCtaSmem);
   if (attr != cudaSuccess) return attr;
-  return launch_kernel(k_w8a16_f8<TT>, dim3((unsigned)units, 1, (unsigned)p.splits), dim3(C::THREADS),
-                       C::smem_bytes(p.stages), st, (unsigned)p.splits, tw, tx, p);
+  return launch_kernel(k_w8a16_f8<TMAX>, dim3((unsigned)units, 1, (unsigned)p.splits), dim3(C::THREADS),
+                       C::smem_bytes(tt, p.stages), st, (unsigned)p.splits, tw, tx, p);
 }
 
 }  // namespace
 
 // Token tile.  Up to kW8A16F8MaxM = 32 tokens: beyond that the E4M3 terms of
 // the tile (4 tt x 128 bytes a k-block) outweigh the weight tile they meet,
-// and the BF16 path with converted weights is faster.
-int w8a16_f8_tt(int64_t M) { return M <= 16 ? 16 : 32; }
+// and the BF16 path with converted weights is faster.  Up to 16 tokens the
+// tile is the least of 4, 8 and 16 that holds them (k_w8a16_f8<16>).
+int w8a16_f8_tt(int64_t M) { return M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32; }
 
 // K splits (a cluster of at most 8 CTAs): as many as fit two CTAs to an SM,
 // and at least 4 k-blocks of 128 per CTA.  A CTA's stream rate is bounded by
@@ -518,7 +533,7 @@ cudaError_t launch_w8a16_f8(const GemmArgs &g, void *ws, const DeviceInfo &dev, 
   const int64_t tt = w8a16_f8_tt(g.M), ttiles = (g.M + tt - 1) / tt;
   uint8_t *xs = (uint8_t *)ws;
   float *xscale = (float *)((uint8_t *)ws + (ttiles * kSplitTerms * tt * g.K + 255) / 256 * 256);
-  return tt == 16 ? launch_tt<16>(g, xs, xscale, dev, st) : launch_tt<32>(g, xs, xscale, dev, st);
+  return tt <= 16 ? launch_tt<16>(g, (int)tt, xs, xscale, dev, st) : launch_tt<32>(g, (int)tt, xs, xscale, dev, st);
 }
 
 }  // namespace qlin

@@ -33,11 +33,12 @@
  *     later work sees its outputs.  Consecutive kernels of the library start
  *     early (programmatic dependent launch): a kernel's CTAs take SMs while its
  *     predecessor finishes, and wait for it before they read its outputs.  The
- *     one input read before that wait is a linear's weight codes (`qw`).  So a
- *     buffer of weight codes must not be the output of the library call right
- *     before the linear on its stream, other than qlin_quantize_weight (which
- *     lets no later kernel start before it completes).  Codes written by any
- *     other kernel or copy, or by any earlier call, are read as written.
+ *     inputs read before that wait are a linear's weights: its codes (`qw`),
+ *     their scales (`w_scale`) and its bias.  So none of these may be the
+ *     output of the library call right before the linear on its stream, other
+ *     than qlin_quantize_weight (which lets no later kernel start before it
+ *     completes).  Weights written by any other kernel or copy, or by any
+ *     earlier call, are read as written.
  *   - Argument errors are detected on the host before anything is launched and
  *     returned as a status: NULL required pointer, negative sizes, K or N not a
  *     multiple of 16, pointers not 16-byte aligned, unknown qtype, workspace

@@ -70,8 +70,8 @@ def test_w8a16_gate_up_silu(capi, qt, M, K, I):
     w8a16_glu(capi, qt, M, K, I, M % 2 == 0, "a")
 
 
-@pytest.mark.parametrize("M,K,I", [(1, 1040, 384), (8, 3584, 256), (16, 3584, 128), (29, 528, 2048),
-                                   (32, 2048, 640)])
+@pytest.mark.parametrize("M,K,I", [(1, 1040, 384), (3, 3584, 256), (6, 18944, 128), (8, 3584, 256),
+                                   (16, 3584, 128), (29, 528, 2048), (32, 2048, 640)])
 def test_w8a16_gate_up_silu_e4m3_fp8_path(capi, M, K, I):
     """E4M3 up to 32 tokens: a weight tile is 64 gate rows and their 64 up rows,
     so gate and up meet in one partial tile before silu(g) * u is formed."""

@@ -71,15 +71,15 @@ def test_w8a16_ragged_kn(capi, qt, M, K, N):
     w8a16_case(capi, qt, M, K, N, M % 2 == 1, "ragged-kn", outliers=True)
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 16, 16), (2, 1040, 1040), (5, 18944, 64), (8, 2064, 400), (7, 128, 3584),
-                                   (13, 528, 2064), (16, 18944, 64), (17, 3584, 4096),
-                                   (25, 2064, 400), (32, 3600, 4112), (31, 128, 3584)])
+@pytest.mark.parametrize("M,K,N", [(1, 16, 16), (2, 1040, 1040), (3, 18944, 64), (4, 2064, 400), (5, 18944, 64),
+                                   (8, 2064, 400), (7, 128, 3584), (13, 528, 2064), (16, 18944, 64),
+                                   (17, 3584, 4096), (25, 2064, 400), (32, 3600, 4112), (31, 128, 3584)])
 def test_w8a16_e4m3_fp8_path_edges(capi, M, K, N):
     """Up to 32 tokens E4M3 W8A16 runs as FP8 MMAs on the weight codes against
-    the activations split into E4M3 terms: both token-tile widths (16, 32) and
-    their ragged tails, K not a multiple of 128 (and K = 16), N not a multiple
-    of the 128-row weight tile, and 1- to 8-way K splits whose partial tiles
-    are summed through the cluster's shared memory."""
+    the activations split into E4M3 terms: every token-tile width (4, 8, 16,
+    32) full and with ragged tails, K not a multiple of 128 (and K = 16), N not
+    a multiple of the 128-row weight tile, and 1- to 8-way K splits whose
+    partial tiles are summed through the cluster's shared memory."""
     assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, "e4m3", M, K, N).startswith("k_w8a16_split+k_w8a16_f8<")
     w8a16_case(capi, "e4m3", M, K, N, M % 2 == 1, "f8", outliers=True)
 
