@@ -744,10 +744,16 @@ struct DqCfg {
   //   raw ring      (3 converter quads)               R  % 3 == 0
   //   TMEM A ring   (3 quads wait a_empty, issuers     NA % (3 x ISSUERS) == 0
   //                  wait a_full)
-  //   activations   (ISSUERS MMA threads)             X  % ISSUERS == 0
+  //   activations   (QX: the 3 quads wait x_full)      X  % 3 == 0
+  //                 (else: ISSUERS MMA threads)        X  % ISSUERS == 0
+  // QX: a quad hands a block to the MMA (a_full) only once both its converted
+  // weights are in tensor memory and the block's activation tile has landed,
+  // so an issuer waits on one barrier per block.  256-token tiles keep four
+  // 32 KB activation stages (three were measured slower) and the issuer's own
+  // wait for them.
   static constexpr int NA = TSUM ? 3 : ACOL == 128 ? 12 : 6;  // A stages, 32 columns (64 BF16 k) each
-  //   activations   (fused I8: the 3 quads wait x_full too) X % (QUADS * ISSUERS) == 0
-  static constexpr int X = MODE == 3 ? (BNT <= 32 ? 18 : 12) : BNT <= 32 ? 16 : BNT == 64 ? 8 : BNT == 128 ? 8 : 4;
+  static constexpr int X = MODE == 3 ? (BNT <= 32 ? 18 : 12) : BNT <= 32 ? 18 : BNT == 64 ? 9 : BNT == 128 ? 6 : 4;
+  static constexpr bool QX = X % QUADS == 0;
   static constexpr int RING = 200 * 1024;
   static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
   static constexpr int R = (R0 > 15 ? 15 : R0) / 3 * 3;  // raw stages
@@ -759,8 +765,8 @@ struct DqCfg {
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
   static_assert(R % QUADS == 0 && R >= 6, "raw ring depth: multiple of the converter quads");
   static_assert(NA % (QUADS * ISSUERS) == 0, "A ring depth: multiple of quads x issuers");
-  static_assert(X % ISSUERS == 0, "activation ring depth: multiple of the MMA issuers");
-  static_assert(MODE != 3 || X % (QUADS * ISSUERS) == 0, "fused activation ring: multiple of quads x issuers");
+  static_assert(QX ? X % QUADS == 0 : X % ISSUERS == 0, "activation ring depth: multiple of its waiters");
+  static_assert(MODE != 3 || QX, "fused quantization: the quads wait for the activation tiles");
   static_assert(ND * DSTRIDE <= ACOL && ACOL + NA * 32 <= 512, "TMEM columns");
   static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -996,8 +1002,8 @@ __global__ void __launch_bounds__(640, 1)
           for (int kb = cb + e; kb < ce; kb += C::ISSUERS) {
             const int i = j * nkb + kb;  // block index within this CTA
             const int sx = i % C::X, sa = i % C::NA;
-            if (!mbar_wait(&x_full[sx], (i / C::X) & 1, abort_flag) ||
-                !mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {
+            if ((!C::QX && !mbar_wait(&x_full[sx], (i / C::X) & 1, abort_flag)) ||
+                !mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {  // QX: a_full covers both
               ok = false;
               break;
             }
@@ -1081,6 +1087,11 @@ __global__ void __launch_bounds__(640, 1)
       }
       tmem_st32(tmem + lane_base + C::ACOL + sa * 32, words);
       tmem_st_wait();
+      // the block's activation tile (already waited for when quantized in place)
+      if (C::QX && !kXQ && !mbar_wait(&x_full[i % C::X], (i / C::X) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[sa]);
