@@ -745,15 +745,19 @@ struct DqCfg {
   //   TMEM A ring   (3 quads wait a_empty, issuers     NA % (3 x ISSUERS) == 0
   //                  wait a_full)
   //   activations   (QX: the 3 quads wait x_full)      X  % 3 == 0
-  //                 (else: ISSUERS MMA threads)        X  % ISSUERS == 0
-  // QX: a quad hands a block to the MMA (a_full) only once both its converted
-  // weights are in tensor memory and the block's activation tile has landed,
-  // so an issuer waits on one barrier per block.  256-token tiles keep four
-  // 32 KB activation stages (three were measured slower) and the issuer's own
-  // wait for them.
+  // An issuer waits on one barrier per block, a_full, which completes only once
+  // both the block's converted weights are in tensor memory and its
+  // activation tile has landed:
+  //   XA (X <= NA, no in-place quantization): the activation tile's TMA
+  //      completes on the block's a_full itself (one more arrival, with its
+  //      bytes).  The load of block i follows the MMA of block i - X, so the
+  //      issuers have consumed a_full's previous phase (block i - NA) by then.
+  //   QX: the converter quad waits for the tile (x_full) before it arrives.
+  // 256-token tiles keep four 32 KB activation stages (three were slower).
   static constexpr int NA = TSUM ? 3 : ACOL == 128 ? 12 : 6;  // A stages, 32 columns (64 BF16 k) each
   static constexpr int X = MODE == 3 ? (BNT <= 32 ? 18 : 12) : BNT <= 32 ? 18 : BNT == 64 ? 9 : BNT == 128 ? 6 : 4;
-  static constexpr bool QX = X % QUADS == 0;
+  static constexpr bool XA = MODE != 3 && X <= NA;
+  static constexpr bool QX = !XA;
   static constexpr int RING = 200 * 1024;
   static constexpr int R0 = (RING - X * X_BYTES) / RAW_BYTES;
   static constexpr int R = (R0 > 15 ? 15 : R0) / 3 * 3;  // raw stages
@@ -765,8 +769,7 @@ struct DqCfg {
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
   static_assert(R % QUADS == 0 && R >= 6, "raw ring depth: multiple of the converter quads");
   static_assert(NA % (QUADS * ISSUERS) == 0, "A ring depth: multiple of quads x issuers");
-  static_assert(QX ? X % QUADS == 0 : X % ISSUERS == 0, "activation ring depth: multiple of its waiters");
-  static_assert(MODE != 3 || QX, "fused quantization: the quads wait for the activation tiles");
+  static_assert(XA || X % QUADS == 0, "activation ring depth: multiple of the quads that wait on it");
   static_assert(ND * DSTRIDE <= ACOL && ACOL + NA * 32 <= 512, "TMEM columns");
   static_assert(BM * BNT * 4 <= BAR_OFF, "split-K partial tile must fit the rings");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -910,7 +913,7 @@ __global__ void __launch_bounds__(640, 1)
     else if (t < B1) bar = &raw_empty[t - B0], cnt = 4;  // the four warps of the quad that read it
     else if (t < B2) bar = &x_full[t - B1];
     else if (t < B3) bar = &x_empty[t - B2];
-    else if (t < B4) bar = &a_full[t - B3], cnt = 4;     // the converter quad
+    else if (t < B4) bar = &a_full[t - B3], cnt = C::XA ? 5 : 4;  // the converter quad (+ the activation tile)
     else if (t < B5) bar = &a_empty[t - B4];
     else if (t < B6) bar = &acc_full[t - B5], cnt = C::ISSUERS;  // one commit per MMA issuer
     else if (t < B7) bar = &acc_empty[t - B6], cnt = 4;          // the epilogue quad
@@ -973,11 +976,17 @@ __global__ void __launch_bounds__(640, 1)
             *abort_flag = 1;
             break;
           }
-          mbar_arrive_expect_tx(&x_full[s], C::X_BYTES);
-          tma_load_2d(&tm_x, &x_full[s], xs + s * C::X_BYTES, (kb0 + kb) * C::BK, m0);
+          uint64_t *bar = C::XA ? &a_full[i % C::NA] : &x_full[s];
+          mbar_arrive_expect_tx(bar, C::X_BYTES);
+          tma_load_2d(&tm_x, bar, xs + s * C::X_BYTES, (kb0 + kb) * C::BK, m0);
         }
       }
-      if (*abort_flag) drain_ring(x_full, C::X, i, C::X);  // abort: armed stages land first
+      // abort: armed stages land first (XA: the last X blocks' a_full phases, bounded
+      // waits that may also run out for want of the quads' arrivals)
+      if (*abort_flag) {
+        if (C::XA) drain_ring(a_full, C::NA, i, C::X);
+        else drain_ring(x_full, C::X, i, C::X);
+      }
     }
   } else if (warp == 1 || (warp == 3 && C::ISSUERS == 2)) {  // -- MMA issuers
     // Issuer e (warp 1: e = 0, warp 3: e = 1) takes the k-blocks with kb % ISSUERS == e
@@ -1002,8 +1011,7 @@ __global__ void __launch_bounds__(640, 1)
           for (int kb = cb + e; kb < ce; kb += C::ISSUERS) {
             const int i = j * nkb + kb;  // block index within this CTA
             const int sx = i % C::X, sa = i % C::NA;
-            if ((!C::QX && !mbar_wait(&x_full[sx], (i / C::X) & 1, abort_flag)) ||
-                !mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {  // QX: a_full covers both
+            if (!mbar_wait(&a_full[sa], (i / C::NA) & 1, abort_flag)) {  // weights and activations
               ok = false;
               break;
             }
@@ -1088,7 +1096,7 @@ __global__ void __launch_bounds__(640, 1)
       tmem_st32(tmem + lane_base + C::ACOL + sa * 32, words);
       tmem_st_wait();
       // the block's activation tile (already waited for when quantized in place)
-      if (C::QX && !kXQ && !mbar_wait(&x_full[i % C::X], (i / C::X) & 1, abort_flag)) {
+      if (C::QX && !kXQ && !mbar_wait(&x_full[i % C::X], (i / C::X) & 1, abort_flag)) {  // XA: on a_full
         ok = false;
         break;
       }
