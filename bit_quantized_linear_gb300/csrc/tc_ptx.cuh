@@ -128,6 +128,12 @@ __device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap *tm, uint64_t
 
 // Brings the box at (c0, c1) into L2 ahead of its tiled load (no completion
 // to wait for, no shared memory).
+// Pulls the 128-byte line holding `p` into L2 (no data is returned).  L2 is the
+// GPU's point of coherence, so a line fetched while another kernel may still be
+// writing it is never read stale: later writes update it in L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *tm, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
                "r"(c0), "r"(c1)

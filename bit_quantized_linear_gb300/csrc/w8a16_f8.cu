@@ -119,15 +119,24 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
     if (threadIdx.x == 0 && c == 0) set_status(status, QLIN_ERR_UNSUPPORTED);
     return;
   }
+  const int m = blockIdx.y, n8 = K / 8;  // K % 16 == 0
+  const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
+  const int u0 = c * per, u1 = min(n8, u0 + per);
+  // While the previous kernel finishes: pull this chunk of the row into L2 (a
+  // prefetch returns nothing, so it reads no value before the wait below), so
+  // that the loads after the wait do not queue behind the next linear's
+  // weight traffic in HBM.
+#pragma unroll
+  for (int i = 0; i < kSplitMaxPer; ++i) {
+    const int u = u0 + (int)threadIdx.x + i * kSplitThreads;
+    if (u < u1 && (u & 7) == 0) prefetch_l2(row + u);  // one per 128-byte line
+  }
   // The FP8 linear that follows may start at once: before its own wait for this
   // kernel it only arms barriers and loads weight tiles, so its CTAs take the
   // SMs that the previous linear frees during its tail.  Nothing here is
   // read or written before the previous kernel has completed.
   pdl_trigger();
   pdl_wait();
-  const int m = blockIdx.y, n8 = K / 8;  // K % 16 == 0
-  const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
-  const int u0 = c * per, u1 = min(n8, u0 + per);
   uint4 v[kSplitMaxPer];
   float a = 0.0f;
 #pragma unroll
