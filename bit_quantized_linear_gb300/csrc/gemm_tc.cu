@@ -972,7 +972,12 @@ __global__ void __launch_bounds__(640, 1)
         const int m0 = ((blockIdx.x + j * G) / p.ntiles) * BNT;
         for (int kb = 0; kb < nkb; ++kb, ++i) {
           const int s = i % C::X;
-          if (i >= C::X && !mbar_wait(&x_empty[s], ((i / C::X) & 1) ^ 1, abort_flag)) {
+          // the slot is free once the MMA of block i - X is done: XA reads that from
+          // the block's A-stage release (one commit per block serves both rings;
+          // this thread waits on every block's in turn, and X <= NA keeps it within
+          // one phase of each slot)
+          if (i >= C::X && !(C::XA ? mbar_wait(&a_empty[(i - C::X) % C::NA], ((i - C::X) / C::NA) & 1, abort_flag)
+                                   : mbar_wait(&x_empty[s], ((i / C::X) & 1) ^ 1, abort_flag))) {
             *abort_flag = 1;
             break;
           }
@@ -1024,7 +1029,7 @@ __global__ void __launch_bounds__(640, 1)
             mma_bf16_ts(dt, at + 8, bd + 2, C::IDESC, 1u);
             mma_bf16_ts(dt, at + 16, bd + 4, C::IDESC, 1u);
             mma_bf16_ts(dt, at + 24, bd + 6, C::IDESC, 1u);
-            mma_commit(&x_empty[sx]);
+            if (!C::XA) mma_commit(&x_empty[sx]);
             mma_commit(&a_empty[sa]);
             last = i;
           }
@@ -1036,7 +1041,7 @@ __global__ void __launch_bounds__(640, 1)
       // its shared memory (a successor CTA on this SM may already own it); the
       // waits hold on the abort path too
       if (last >= 0) {
-        ok = mbar_wait_drain(&x_empty[last % C::X], (last / C::X) & 1) &&
+        ok = (C::XA || mbar_wait_drain(&x_empty[last % C::X], (last / C::X) & 1)) &&
              mbar_wait_drain(&a_empty[last % C::NA], (last / C::NA) & 1) && ok;
       }
       if (!ok) *abort_flag = 1;

@@ -477,9 +477,10 @@ cudaError_t launch_tt(const GemmArgs &g, int tt, uint8_t *xs, float *xscale, con
   if (!map_u8(&tw, g.qw, g.glu ? 2 * g.N : g.N, g.K, g.glu ? 64 : 128) ||
       !map_u8(&tx, xs, (int64_t)ttiles * NB, g.K, NB))
     return cudaErrorInvalidValue;
-  // one cluster per token row: C CTAs of at most kSplitMaxPer 16-byte pieces per thread
+  // one cluster per token row: C CTAs of about two (at most kSplitMaxPer) 16-byte
+  // pieces per thread (one piece a thread, or four, measured slower)
   const int n8 = (int)(g.K / 8);
-  int chunks = (n8 + kSplitThreads - 1) / kSplitThreads;
+  int chunks = (n8 + 2 * kSplitThreads - 1) / (2 * kSplitThreads);
   if (chunks > kSplitMaxChunks) chunks = kSplitMaxChunks;
   const int per = (n8 + chunks - 1) / chunks;
   if (per > kSplitMaxPer * kSplitThreads) return cudaErrorInvalidValue;  // K beyond 2^17 (refused on the host)
