@@ -1598,7 +1598,14 @@ static cudaError_t launch_dq_t(const GemmArgs &g, const void *xb, const DeviceIn
   if (attr != cudaSuccess) return attr;
   const int ntiles = g.glu ? (int)(g.N / 64) : (int)((g.N + C::BM - 1) / C::BM);
   const int units = ntiles * (int)((g.M + BNT - 1) / BNT);
-  const int S = w8_swap_splits(units, g.K, dev.sms, BNT);
+  int S = w8_swap_splits(units, g.K, dev.sms, BNT);
+  // A unit's splits reduce through their cluster, and every unit's cluster
+  // should be resident in one wave: fewer splits where the GPCs cannot hold
+  // `units` clusters of S CTAs at once (a second wave doubles the call).
+  static std::atomic<int> clusters[kMaxDevices * 9];
+  for (int mc; S > 1 && (mc = max_active_clusters_z(k_w8_dq<BNT, QT, MODE>, dim3(C::THREADS), C::SMEM, (unsigned)S,
+                                                     dev.device, clusters)) > 0 && units > mc;)
+    --S;
   const int G = S > 1 ? units : (units < dev.sms ? units : dev.sms);
   SwapParams p{(int)g.M, (int)g.N, (int)g.K, g.x_scale_per_token, g.glu, S,  units,
                ntiles,    g.w_scale, g.x_scale, g.bias,  g.y,        dev.status};

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "qlin.h"
@@ -105,6 +106,39 @@ cudaError_t launch_kernel_x(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// How many clusters of `cz` CTAs along z (block, dynamic shared memory as
+// given) can be resident on the current device at once; 0 if the query fails.
+// Remembered per device and cluster size in `cache` (kMaxDevices x 9 entries,
+// one table per kernel), since the answer depends only on the kernel's
+// resources and the device.
+constexpr int kMaxDevices = 64;  // devices a process may use (per-device tables)
+template <typename... KArgs>
+int max_active_clusters_z(void (*kernel)(KArgs...), dim3 block, size_t smem, unsigned cz, int device,
+                          std::atomic<int> *cache) {
+  if (cz < 2 || cz > 8 || device < 0 || device >= kMaxDevices) return 0;
+  std::atomic<int> &slot = cache[device * 9 + cz];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, cz);
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = 1;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = cz;
+  cfg.attrs = &a;
+  cfg.numAttrs = 1;
+  n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void *)kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  slot.store(n, std::memory_order_relaxed);
+  return n;
 }
 
 cudaError_t launch_quantize_weight(int qtype, int64_t N, int64_t K, const float *w, void *qw,
