@@ -765,7 +765,10 @@ struct DqCfg {
   // merged gate_up: per 16-token chunk the gate rows pass g of tokens 8..15 and the up
   // rows u of tokens 0..7 to each other; two slots, so a side can run one chunk ahead
   static constexpr int XCHG_OFF = BAR_OFF + 1024, XCHG_BYTES = 2 * 2 * 8 * 64 * 4;
-  static constexpr int SMEM = XCHG_OFF + XCHG_BYTES + 1024;  // + alignment slack
+  // split-K: the tile's per-row weight scales and biases and per-token scales,
+  // staged while the main loop runs
+  static constexpr int SCL_OFF = XCHG_OFF + XCHG_BYTES, SCL_BYTES = (2 * BM + BNT) * 4;
+  static constexpr int SMEM = SCL_OFF + SCL_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t IDESC = umma_idesc(1, 1, BM, BNT);
   static_assert(R % QUADS == 0 && R >= 6, "raw ring depth: multiple of the converter quads");
   static_assert(NA % (QUADS * ISSUERS) == 0, "A ring depth: multiple of quads x issuers");
@@ -816,12 +819,13 @@ __device__ __forceinline__ void convert16(uint4 raw, uint32_t *o) {
 
 // Writes 4 consecutive output channels of one token row (S > 1 path).
 template <int MODE>
-__device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const uint32_t (&v)[4]) {
+// sw, b: the four channels' weight scales and biases; sx: the token's scale
+// (staged in shared memory by the caller).
+__device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const uint32_t (&v)[4], const float *sw,
+                                       const float *b, float sx) {
   if constexpr (MODE == kSwapI8Raw) {
     *reinterpret_cast<uint4 *>((int32_t *)p.y + (size_t)m * p.N + n) = make_uint4(v[0], v[1], v[2], v[3]);
   } else {
-    const float sx = MODE == kSwapI8Scaled || MODE == kSwapI8Fused ? __ldg(p.x_scale + (p.xs_per_token ? m : 0))
-                                                                     : 1.0f;
     uint32_t o[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -830,8 +834,8 @@ __device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const 
       for (int e = 0; e < 2; ++e) {
         const int k = 2 * h + e;
         const float acc = MODE == kSwapW8A16 ? __uint_as_float(v[k]) : (float)(int)v[k];
-        a[e] = acc * (sx * __ldg(p.w_scale + n + k));
-        if (p.bias) a[e] += bf16_bits_to_f32(__ldg(p.bias + n + k));
+        a[e] = acc * (sx * sw[k]);
+        if (p.bias) a[e] += b[k];
       }
       o[h] = pack_bf16x2(a[0], a[1]);
     }
@@ -841,20 +845,20 @@ __device__ __forceinline__ void store4(const SwapParams &p, int m, int n, const 
 
 // Merged gate_up (S > 1 path): 4 consecutive output channels of one token row
 // from the summed gate and up accumulators: y = silu(gate) * up.
+// swg, bg4 / swu, bu4: the gate and up channels' weight scales and biases; sx:
+// the token's scale (staged in shared memory by the caller; zero biases when
+// there is no bias).
 template <int MODE>
 __device__ __forceinline__ void glu_store4(const SwapParams &p, int m, int ch, const uint32_t (&g)[4],
-                                           const uint32_t (&u)[4]) {
-  const float sx = MODE == kSwapI8Scaled || MODE == kSwapI8Fused ? __ldg(p.x_scale + (p.xs_per_token ? m : 0))
-                                                                   : 1.0f;
+                                           const uint32_t (&u)[4], const float *swg, const float *bg4,
+                                           const float *swu, const float *bu4, float sx) {
   float y[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float ga = MODE == kSwapW8A16 ? __uint_as_float(g[e]) : (float)(int)g[e];
     const float ua = MODE == kSwapW8A16 ? __uint_as_float(u[e]) : (float)(int)u[e];
-    const float bg = p.bias ? bf16_bits_to_f32(__ldg(p.bias + ch + e)) : 0.0f;
-    const float bu = p.bias ? bf16_bits_to_f32(__ldg(p.bias + p.N + ch + e)) : 0.0f;
-    const float gv = fmaf(ga, sx * __ldg(p.w_scale + ch + e), bg);
-    const float uv = fmaf(ua, sx * __ldg(p.w_scale + p.N + ch + e), bu);
+    const float gv = fmaf(ga, sx * swg[e], bg4[e]);
+    const float uv = fmaf(ua, sx * swu[e], bu4[e]);
     y[e] = silu_f(gv) * uv;
   }
   *reinterpret_cast<uint2 *>((uint16_t *)p.y + (size_t)m * p.N + ch) =
@@ -885,6 +889,7 @@ __global__ void __launch_bounds__(640, 1)
   uint32_t *tmem_slot = (uint32_t *)(u_taken + 2);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
   float *xchg = reinterpret_cast<float *>(smem + C::XCHG_OFF);
+  float *scl_w = reinterpret_cast<float *>(smem + C::SCL_OFF), *scl_b = scl_w + C::BM, *scl_x = scl_b + C::BM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.z, S = p.splits;
   // The split-K reduction reads the partial tiles of S cluster peers through
@@ -1114,6 +1119,20 @@ __global__ void __launch_bounds__(640, 1)
     const int q4 = warp & 3, nl = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     const bool up_row = p.glu && nl >= 64;  // merged gate_up: TMEM lanes 64..127 hold the up rows
+    if (S > 1) {
+      // Split-K (one unit per CTA): the factors the cluster's sum applies, read
+      // while the main loop runs instead of after the sum.
+      const int u = blockIdx.x, tn = u % p.ntiles, mu = (u / p.ntiles) * BNT;
+      const int ch = p.glu ? (up_row ? p.N + tn * 64 + (nl - 64) : tn * 64 + nl) : tn * C::BM + nl;
+      const bool in = p.glu || ch < p.N;
+      // (the raw int32 form has no factors: its scale pointers are null)
+      scl_w[nl] = MODE != kSwapI8Raw && in ? __ldg(p.w_scale + ch) : 0.0f;
+      scl_b[nl] = MODE != kSwapI8Raw && in && p.bias ? bf16_bits_to_f32(__ldg(p.bias + ch)) : 0.0f;
+      for (int t = nl; t < BNT; t += 128)
+        scl_x[t] = MODE == kSwapI8Scaled || MODE == kSwapI8Fused
+                       ? (p.xs_per_token ? (mu + t < p.M ? __ldg(p.x_scale + mu + t) : 0.0f) : __ldg(p.x_scale))
+                       : 1.0f;
+    }
     int cidx = 0, xround = 0;
     bool ok = true;
     // Writes the outputs of this thread's row for tokens m0 + c .. m0 + c + 15 from
@@ -1182,6 +1201,18 @@ __global__ void __launch_bounds__(640, 1)
       const int wrow = !p.glu ? tt * C::BM + nl : (up_row ? p.N + tt * 64 + (nl - 64) : tt * 64 + nl);
       const int ochan = p.glu ? tt * 64 + (nl & 63) : wrow;
       const bool valid = p.glu ? true : wrow < p.N;
+      // this row's factors (used without split-K), read before the accumulator
+      // wait where the registers allow (not beside 64 int32 sums)
+      constexpr bool kEarly = !(kI8 && !C::TSUM && BNT >= 64);
+      // (the raw int32 form has no factors: its scale pointers are null)
+      auto row_factors = [&](float &sw, float &b, float &sx) {
+        constexpr bool kScaled = MODE != kSwapI8Raw;
+        sw = kScaled && S == 1 && valid ? __ldg(p.w_scale + wrow) : 0.0f;
+        b = kScaled && S == 1 && valid && p.bias ? bf16_bits_to_f32(__ldg(p.bias + wrow)) : 0.0f;
+        sx = kScaled && kI8 && S == 1 ? __ldg(p.x_scale) : 1.0f;
+      };
+      float sw_u = 0.0f, b_u = 0.0f, sx_u = 1.0f;
+      if constexpr (kEarly) row_factors(sw_u, b_u, sx_u);
       constexpr int NSUM = kI8 && !C::TSUM ? BNT : 1;  // int32 sums held in registers
       int32_t sums[NSUM];
 #pragma unroll
@@ -1272,8 +1303,8 @@ __global__ void __launch_bounds__(640, 1)
             }
           }
         } else if (S == 1) {
-          const float sw = valid ? __ldg(p.w_scale + wrow) : 0.0f;
-          const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + wrow)) : 0.0f;
+          if constexpr (!kEarly) row_factors(sw_u, b_u, sx_u);
+          const float sw = sw_u, b = b_u;
           if constexpr (C::NACC == 1) {
             // double-buffered: the next 16 columns are loaded while these are stored
             uint32_t ra[16], rb[16];
@@ -1345,9 +1376,8 @@ __global__ void __launch_bounds__(640, 1)
                   if (valid && m0 + c + e < p.M) ((int32_t *)p.y)[(size_t)(m0 + c + e) * p.N + wrow] = s16[e];
               }
             } else {
-              const float sw = valid ? __ldg(p.w_scale + wrow) : 0.0f;
-              const float sx0 = __ldg(p.x_scale);
-              const float b = (valid && p.bias) ? bf16_bits_to_f32(__ldg(p.bias + wrow)) : 0.0f;
+              if constexpr (!kEarly) row_factors(sw_u, b_u, sx_u);
+              const float sw = sw_u, sx0 = sx_u, b = b_u;
 #pragma unroll
               for (int c = 0; c < BNT; c += 16) {  // fully unrolled: sums[] stays in registers
                 if (ok) {
@@ -1421,7 +1451,9 @@ __global__ void __launch_bounds__(640, 1)
           }
         }
         const int m = m0 + jj;
-        if (m < p.M) glu_store4<MODE>(p, m, tt * 64 + nq, ag, au);
+        if (m < p.M)
+          glu_store4<MODE>(p, m, tt * 64 + nq, ag, au, scl_w + nq, scl_b + nq, scl_w + 64 + nq, scl_b + 64 + nq,
+                           scl_x[jj]);
       }
     } else if (warp >= 4) {
       const int ct = threadIdx.x - 128;  // 512 threads
@@ -1451,7 +1483,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         const int e0 = 4 * w4, jj = e0 / C::BM, nl = e0 % C::BM;
         const int m = m0 + jj, n = n0 + nl;
-        if (m < p.M && n < p.N) store4<MODE>(p, m, n, acc);
+        if (m < p.M && n < p.N) store4<MODE>(p, m, n, acc, scl_w + nl, scl_b + nl, scl_x[jj]);
       }
     }
     cluster_sync();  // no CTA leaves while a peer may still read its shared memory
