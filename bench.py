@@ -55,7 +55,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def workload_calls(name: str):
     """List of synth.Linear describing one step of the workload."""
     if name == "decode7b":
-        return synth.workload(synth.DECODE7B).linears, synth.DECODE7B
+        # The sweep's calls are independent, and a step issues them largest batch
+        # first: the calls with the most output bytes then copy their results back
+        # to the host while the smaller ones run (the end-to-end pass); the
+        # device-resident step is the same set of calls in any order.
+        lins = sorted(synth.workload(synth.DECODE7B).linears, key=lambda l: -l.M)
+        return lins, synth.DECODE7B
     if name == "small":
         return synth.workload(synth.SMALL).linears, synth.SMALL
     if name == "w8a8-3b":
