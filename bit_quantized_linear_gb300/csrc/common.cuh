@@ -85,6 +85,22 @@ __device__ __forceinline__ uint8_t quantize_one(float x, const Scale &c) {
   }
 }
 
+// The INT8 code of x under a run-time (static) scale, as the integer-valued
+// float the BF16 MMA consumes: the same code as quantize_one<QLIN_INT8, false>
+// (the same quotient, round half to even, clamp to [-127, 127]) without the
+// round trip through an integer.  The copysign of quotient() only matters for
+// quotients that round to zero, and a zero code is returned as +0 either way.
+__device__ __forceinline__ float quantize_i8_value(float x, const Scale &c) {
+  float v;
+  if (c.fast) {
+    const float q = fminf(fmaxf(__fmul_rn(x, c.r), -0x1p32f), 0x1p32f);
+    v = __fmaf_rn(__fmaf_rn(-q, c.s, x), c.r, q);
+  } else {
+    v = __fdiv_rn(x, c.s);
+  }
+  return fminf(fmaxf(rintf(v), -127.0f), 127.0f) + 0.0f;
+}
+
 // ------------------------------------------------ static E4M3, eight at a time
 // The static E4M3 quantizer of a whole tensor (one run-time scale s) gives the
 // same codes as quantize_one<QLIN_E4M3, false> for every finite input, with

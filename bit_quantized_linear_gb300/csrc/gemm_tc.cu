@@ -1091,8 +1091,8 @@ __global__ void __launch_bounds__(640, 1)
           uint32_t o[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float lo = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(w[e] & 0xFFFFu), xsc);
-            const float hi = (float)(int8_t)quantize_one<QLIN_INT8, false>(bf16_bits_to_f32(w[e] >> 16), xsc);
+            const float lo = quantize_i8_value(bf16_bits_to_f32(w[e] & 0xFFFFu), xsc);
+            const float hi = quantize_i8_value(bf16_bits_to_f32(w[e] >> 16), xsc);
             o[e] = pack_code_bf16x2(lo, hi);
           }
           sts128(xb + 16 * c, make_uint4(o[0], o[1], o[2], o[3]));

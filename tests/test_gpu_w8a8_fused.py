@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from bit_quantized_linear_gb300 import synth
-from _helpers import check_tol, from_dev_bf16, to_dev, to_dev_bf16
+from _helpers import bf16_to_f64, check_tol, from_dev_bf16, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -158,3 +158,34 @@ def test_fused_e4m3_codes_bitexact(capi, M, K, N):
     bad = np.argwhere(got != ref)
     assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:4].tolist()}"
     assert (ref == 0x80).any() and (ref == 0xFE).any()  # -0 and -448 both occur
+
+
+@pytest.mark.parametrize("M", [1, 16, 33, 64])
+def test_fused_int8_codes_bitexact(capi, M):
+    """The codes the fused kernel quantizes in place, read back bit for bit: an
+    identity weight (code 1 on the diagonal, scale 1, no bias) makes every output
+    y[m, n] = code[m, n] * s_x, and with s_x = 2^-4 that product is exact in BF16.
+    The activations include exact ties (half-integers times s_x, which round to
+    even), values beyond the clamp (N(0, 9) spans +-48 s_x per sigma, and +-300),
+    zeros and negative zeros; the codes must equal the oracle's."""
+    K = N = 512
+    sx = np.float32(2.0 ** -4)
+    rng = synth.rng_for("test-w8a8-fused", 0, f"codes-{M}", "all")
+    xf = (rng.standard_normal((M, K)) * 3.0).astype(np.float32)
+    halves = (rng.integers(-127, 127, size=(M, K)) + 0.5).astype(np.float32) * sx  # exact ties in BF16
+    pick = rng.random((M, K)) < 0.3
+    xf = np.where(pick, halves, xf)
+    xf[:, :4] = np.array([0.0, -0.0, 300.0, -300.0], np.float32)
+    x = synth.f32_to_bf16_bits(xf)
+    qw = np.eye(N, K, dtype=np.int8).view(np.uint8)
+    sw = np.ones(N, np.float32)
+    assert capi.qlin_kernel_name(capi.QLIN_OP_W8A8_LINEAR, "int8", M, K, N).endswith(",i8,xq>")
+    y = capi.w8a8_linear("int8", to_dev_bf16(x), to_dev(np.array([sx], np.float32)), to_dev(qw), to_dev(sw), None)
+    torch.cuda.synchronize()
+    assert capi.qlin_get_device_status() == capi.QLIN_OK
+    codes = bf16_to_f64(from_dev_bf16(y)) / float(sx)
+    assert np.all(codes == np.round(codes))
+    ref = oracle.quantize_act(oracle.INT8, x, sx).view(np.int8).astype(np.float64)
+    bad = np.argwhere(codes != ref)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:4].tolist()}"
+    assert (np.abs(ref) == 127).any() and (ref == 0).any()
