@@ -105,3 +105,11 @@ def test_gate_up_silu_zero_tokens(capi):
     n0 = capi.qlin_launch_count()
     y = capi.w8a16_gate_up_silu("int8", x, q, s)
     assert y.shape == (0, I) and capi.qlin_launch_count() == n0
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+def test_w8a16_gate_up_silu_partial_last_wave(capi, qt):
+    """Merged gate_up with a mostly empty last wave of units (I = 11008 at 256
+    tokens: 344 units of 64 gate + 64 up rows on 152 persistent CTAs).  Full
+    output against the oracle."""
+    w8a16_glu(capi, qt, 256, 2048, 11008, True, "last-wave")

@@ -437,3 +437,12 @@ def test_w8a16_reads_every_weight_code_exactly(capi, qt):
         table = np.array([oracle.e4m3_decode(c) for c in range(256)])
         want = table[q].T
     assert np.array_equal(y, want[:M]), int((y != want[:M]).sum())
+
+
+@pytest.mark.parametrize("qt", ["int8", "e4m3"])
+@pytest.mark.parametrize("M,K,N", [(256, 1024, 22016), (200, 2048, 19712)])
+def test_w8a16_partial_last_wave(capi, qt, M, K, N):
+    """More weight-tile units than SMs with a mostly empty last wave (344 units
+    of 128 x 128 at 256 tokens; 308 at 200 tokens, a ragged token tile): the
+    persistent CTAs take three units or two.  Full output against the oracle."""
+    w8a16_case(capi, qt, M, K, N, M % 2 == 0, "last-wave")
