@@ -98,9 +98,9 @@ __device__ __forceinline__ void split_pair(uint32_t word, float r, uint32_t (&c)
   c[0] = (uint32_t)h1 & a, c[1] = (uint32_t)h2 & a, c[2] = (uint32_t)h1 & b, c[3] = (uint32_t)h2 & b;
 }
 
-// Token row m: one cluster of gridDim.x CTAs, CTA c over pieces [c P, c P + P)
-// of the row (P = `per` 16-byte pieces of 8 elements; each thread holds up to
-// kSplitMaxPer of them in registers).  Each CTA takes the abs-max of its own
+// Token row m: one cluster of gridDim.x CTAs (or one CTA without a cluster),
+// CTA c over pieces [c P, c P + P) of the row (P = `per` 16-byte pieces of 8
+// elements; each thread holds up to kSplitMaxPer of them in registers).  Each CTA takes the abs-max of its own
 // chunk and stores it into every CTA of the cluster (distributed shared
 // memory); after one cluster barrier each CTA has the row's maximum, so the
 // row is read once in all.  Each CTA then writes its chunk's four E4M3 terms
@@ -149,15 +149,21 @@ __global__ void __launch_bounds__(kSplitThreads) k_w8a16_split(const uint16_t *_
   a = warp_max(a);
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = a;
   __syncthreads();
-  if (threadIdx.x < C) {  // this chunk's maximum into CTA threadIdx.x of the cluster
-    float cm = wmax[0];
+  if (C == 1) {  // the whole row in this CTA: no exchange
+    a = wmax[0];
 #pragma unroll
-    for (int w = 1; w < kSplitThreads / 32; ++w) cm = fmaxf(cm, wmax[w]);
-    st_dsmem_f32(map_peer_smem(smem_u32(&cmax[c]), threadIdx.x), cm);
+    for (int w = 1; w < kSplitThreads / 32; ++w) a = fmaxf(a, wmax[w]);
+  } else {
+    if (threadIdx.x < C) {  // this chunk's maximum into CTA threadIdx.x of the cluster
+      float cm = wmax[0];
+#pragma unroll
+      for (int w = 1; w < kSplitThreads / 32; ++w) cm = fmaxf(cm, wmax[w]);
+      st_dsmem_f32(map_peer_smem(smem_u32(&cmax[c]), threadIdx.x), cm);
+    }
+    cluster_sync();  // every chunk's maximum has arrived
+    a = cmax[0];
+    for (int q = 1; q < C; ++q) a = fmaxf(a, cmax[q]);
   }
-  cluster_sync();  // every chunk's maximum has arrived
-  a = cmax[0];
-  for (int q = 1; q < C; ++q) a = fmaxf(a, cmax[q]);
   const float s = split_scale(a), r = 1.0f / s;  // powers of two: exact
   if (c == 0 && threadIdx.x == 0) xscale[m] = s;
   const int j = m / tt, t = m % tt;
@@ -484,9 +490,13 @@ cudaError_t launch_tt(const GemmArgs &g, int tt, uint8_t *xs, float *xscale, con
   if (chunks > kSplitMaxChunks) chunks = kSplitMaxChunks;
   const int per = (n8 + chunks - 1) / chunks;
   if (per > kSplitMaxPer * kSplitThreads) return cudaErrorInvalidValue;  // K beyond 2^17 (refused on the host)
-  cudaError_t e = launch_kernel_x(k_w8a16_split, dim3((unsigned)chunks, (unsigned)g.M), dim3(kSplitThreads), 0, st,
-                                  (unsigned)chunks, (const uint16_t *)g.a, (int)g.M, (int)g.K, tt, per, xs, xscale,
-                                  dev.status);
+  // a row that fits one CTA needs no cluster
+  cudaError_t e =
+      chunks == 1 ? launch_kernel(k_w8a16_split, dim3(1u, (unsigned)g.M), dim3(kSplitThreads), 0, st, 1u,
+                                  (const uint16_t *)g.a, (int)g.M, (int)g.K, tt, per, xs, xscale, dev.status)
+                  : launch_kernel_x(k_w8a16_split, dim3((unsigned)chunks, (unsigned)g.M), dim3(kSplitThreads), 0, st,
+                                    (unsigned)chunks, (const uint16_t *)g.a, (int)g.M, (int)g.K, tt, per, xs, xscale,
+                                    dev.status);
   if (e != cudaSuccess) return e;
   W8F8Params p;
   p.M = (int)g.M;
