@@ -192,3 +192,18 @@ def test_noalloc_reports_as_the_workspace_entry_point(capi):
         for args in [(1, 0, 64, 64, None, good, good, good, None, None), (0, 4, 64, 64, good, good, good, good, None, good)]:
             ws, na = both(*args)
             assert ws == na and ws in (capi.QLIN_ERR_UNSUPPORTED, capi.QLIN_ERR_CUDA), (args, ws, na)
+
+
+def test_fp8_w8a16_token_tiles(capi):
+    """E4M3 W8A16 up to 32 tokens: the split activations take 4 x tt rows of K
+    bytes per token tile of tt tokens (tt = 4, 8, 16 or 32, the least that holds
+    the batch up to 16 tokens), each region rounded up to 256 bytes, and one fp32
+    scale per token."""
+    K = 3584
+    up = lambda b: (b + 255) // 256 * 256
+    for m, tt in [(1, 4), (4, 4), (5, 8), (8, 8), (9, 16), (16, 16), (17, 32), (32, 32)]:
+        tiles = (m + tt - 1) // tt
+        want = up(tiles * 4 * tt * K) + up(4 * m)
+        assert capi.qlin_workspace_bytes(capi.QLIN_OP_W8A16_LINEAR, "e4m3", m, K, 4096) == want, m
+        kernel = "k_w8a16_split+k_w8a16_f8<16>" if m <= 16 else "k_w8a16_split+k_w8a16_f8<32>"
+        assert capi.qlin_kernel_name(capi.QLIN_OP_W8A16_LINEAR, "e4m3", m, K, 4096) == kernel, m
